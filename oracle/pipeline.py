@@ -1,0 +1,106 @@
+"""Whole-path oracle runs -- TEST INFRASTRUCTURE (see the package docstring).
+
+``full_pipeline`` plays every logical rank in turn: plan, expert rows, scatter
+into every destination's receive buffer, completion signalling, then the
+gate-weighted combine of every destination. ``sampled_pipeline`` computes the
+same quantities for a few tokens of one destination only, for workloads too
+large to run in full on the host.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from . import BF16, FP8_1D2D, Plan, combine, default_threads, expert_rows, plan, scatter, signal
+
+SENTINEL_BYTE = 0xFF  # bf16 0xFFFF is a NaN: an unwritten slot cannot pass a value check
+SENTINEL_WORD = np.uint64(0xFFFFFFFFFFFFFFFF)
+
+
+def _dtype_code(dtype: str) -> int:
+    return {"bf16": BF16, "fp8_1d2d": FP8_1D2D}[dtype]
+
+
+def full_pipeline(w, routing, values: list, epoch: int = 1, threads: int | None = None) -> dict:
+    """Run every producer rank, then every destination's combine.
+
+    ``values[r]`` is the operand dict of rank r (``synth.make_rank_values``).
+    Returns plans, rows Y per producer, receive buffers / counts per destination,
+    election counters per producer, signalling logs per producer, slot hit counts
+    per destination and the combined outputs per destination (bf16 bits)."""
+    R, El, k, T, K, N = w.n_ranks, w.n_local_experts, w.top_k, w.tokens, w.K, w.N
+    msg = w.msg_bytes
+    dt = _dtype_code(w.dtype)
+    recv = [np.full(T * k * msg, SENTINEL_BYTE, np.uint8) for _ in range(R)]
+    counts = [np.full(El * R + R, SENTINEL_WORD, np.uint64) for _ in range(R)]
+    hits = np.zeros((R, T * k), np.int32)
+    plans, ys, logs, counters = [], [], [], []
+    bad = 0
+    for r in range(R):
+        pl = plan(R, El, k, routing.topk_ids, r)
+        v = values[r]
+        Y = expert_rows(dt, v["A"], v["W"], pl.expert_offsets, K, N, rows=None,
+                        a_scales=v.get("a_scales"), w_scales=v.get("w_scales"), threads=threads)
+        rows = np.arange(pl.m_total, dtype=np.int64)
+        hits, b = scatter(Y, rows, pl, R, k, N, msg, T, recv, hits)
+        bad += b
+        ctr = np.zeros(R, np.int32)
+        logs.append(signal(R, El, r, pl.send_counts, epoch, counts, ctr))
+        counters.append(ctr)
+        plans.append(pl)
+        ys.append(Y)
+    outs = [combine(recv[d], routing.gates[d], k, N, msg, threads=threads) for d in range(R)]
+    return dict(plans=plans, Y=ys, recv=recv, counts=counts, hits=hits, bad=bad, logs=logs,
+                counters=counters, out=outs)
+
+
+def row_of(pl: Plan, src_rank: int, expert_local: int, t: int, j: int) -> int:
+    """Row of plan ``pl`` that carries routing entry (src_rank, t, j) for a local expert."""
+    lo = int(pl.seg_offsets[expert_local, src_rank])
+    hi = int(pl.seg_offsets[expert_local, src_rank + 1])
+    seg = pl.src_info[lo:hi]
+    hit = np.nonzero((seg[:, 0] == t) & (seg[:, 1] == j))[0]
+    if len(hit) != 1:
+        raise KeyError((src_rank, expert_local, t, j))
+    return lo + int(hit[0])
+
+
+def sampled_pipeline(w, routing, values_of, dst: int, tokens, plans: dict | None = None,
+                     threads: int | None = None) -> dict:
+    """Oracle rows and combined outputs for ``tokens`` of destination ``dst``.
+
+    ``values_of(r)`` returns rank r's operand dict. Returns, per sampled token,
+    the k received rows (bf16 bits [n, k, N]), the producer (rank, row) of each,
+    and the combined output (bf16 bits [n, N])."""
+    R, El, k, N = w.n_ranks, w.n_local_experts, w.top_k, w.N
+    dt = _dtype_code(w.dtype)
+    tokens = np.asarray(tokens, dtype=np.int64)
+    plans = {} if plans is None else plans
+    need: dict[int, list] = {}
+    where = np.zeros((len(tokens), k, 2), np.int64)
+    for i, t in enumerate(tokens):
+        for j in range(k):
+            g = int(routing.topk_ids[dst, t, j])
+            r, e = g // El, g % El
+            if r not in plans:
+                plans[r] = plan(R, El, k, routing.topk_ids, r)
+            m = row_of(plans[r], dst, e, int(t), j)
+            where[i, j] = (r, m)
+            need.setdefault(r, []).append(m)
+    rows_out = np.zeros((len(tokens), k, N), np.uint16)
+    for r, ms in need.items():
+        ms_u = np.unique(np.asarray(ms, dtype=np.int64))
+        v = values_of(r)
+        Y = expert_rows(dt, v["A"], v["W"], plans[r].expert_offsets, w.K, N, rows=ms_u,
+                        a_scales=v.get("a_scales"), w_scales=v.get("w_scales"),
+                        threads=threads or default_threads())
+        pos = {int(m): i for i, m in enumerate(ms_u)}
+        for i in range(len(tokens)):
+            for j in range(k):
+                if where[i, j, 0] == r:
+                    rows_out[i, j] = Y[pos[int(where[i, j, 1])]]
+    # combine over a compact receive buffer holding just these tokens' slots
+    compact = rows_out.reshape(-1).view(np.uint8)
+    g = np.ascontiguousarray(routing.gates[dst][tokens])
+    out = combine(compact, g, k, N, 2 * N, threads=threads)
+    return dict(tokens=tokens, rows=rows_out, where=where, out=out, plans=plans)
