@@ -1,0 +1,241 @@
+/*
+ * moe_ep.h -- C ABI of the fused MoE expert-parallel down-projection:
+ * grouped expert GEMM whose epilogue scatters rows straight into the combine
+ * receive buffers of the token-owning ranks, completion signalling, and the
+ * gate-weighted combine.
+ *
+ * Sources (Modular MAX Mojo API pages):
+ *   "EpiloguePeerSink"     (linalg/matmul/gpu/sm100_structured/structured_kernels/output_writer)
+ *   "P3PeerSendConfig"     (same directory)
+ *   "ep_signal_completion" (shmem/ep_comm)
+ *
+ * General rules.
+ *  - Every entry point is asynchronous on the caller's stream (`ep_stream_t`, a
+ *    cudaStream_t; NULL is the legacy default stream) and returns EP_OK when the
+ *    work was enqueued, or a negative EP_ERR_* code when the host found a problem,
+ *    in which case nothing was launched.
+ *  - The caller allocates and owns every buffer. The library allocates no device
+ *    memory and keeps no per-call state (it caches only the SM count and kernel
+ *    attributes of each device).
+ *  - Problems found on the device (a destination outside the receive buffer, a
+ *    bounded wait that ran out, a plan that does not fit) never trap: the kernel
+ *    ORs an EP_STATUS_* bit into the caller's `status` word, skips the offending
+ *    access and returns. Read the word after the stream has synchronised.
+ *  - All device pointers must be 16-byte aligned.
+ *  - Logical ranks: on one GPU, the receive buffers of the other ranks are simply
+ *    other device allocations; with peer access they may be peer memory.
+ */
+#ifndef MOE_EP_H
+#define MOE_EP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t. */
+typedef struct CUstream_st *ep_stream_t;
+
+/* recv_buf_ptrs on "P3PeerSendConfig" is a StaticTuple of 8 pointers: at most
+ * 8 ranks reachable by direct stores. */
+#define EP_MAX_RANKS 8
+/* Local experts per rank supported by one launch. */
+#define EP_MAX_LOCAL_EXPERTS 256
+
+/* host return codes */
+#define EP_OK 0
+#define EP_ERR_INVALID_ARG (-1)
+#define EP_ERR_UNSUPPORTED (-2)
+#define EP_ERR_CUDA (-3)
+
+/* device status bits, OR-ed into *status */
+#define EP_STATUS_BOUNDS 0x1u   /* a row's destination lay outside the receive buffer: row skipped */
+#define EP_STATUS_TIMEOUT 0x2u  /* a bounded wait ran out (pipeline barrier or rank flag) */
+#define EP_STATUS_CAPACITY 0x4u /* ep_plan: routed rows exceed max_rows; the plan is empty */
+#define EP_STATUS_ROUTING 0x8u  /* ep_plan: an expert id outside [0, n_ranks*n_local_experts) */
+
+/* operand types */
+#define EP_BF16 0     /* bf16 A and W, fp32 accumulation, bf16 rows */
+#define EP_FP8_1D2D 1 /* e4m3 A (1x128 fp32 scales) and W (128x128 fp32 scales), bf16 rows */
+
+/*
+ * Problem description shared by all calls.
+ *   n_ranks              ranks taking part (1..EP_MAX_RANKS)   ["P3PeerSendConfig" n_ranks]
+ *   my_rank              the rank this call plays               ["P3PeerSendConfig" my_rank]
+ *   n_local_experts      experts per rank, E_l; global expert g lives on rank g / E_l at
+ *                        local slot g % E_l                     ["ep_signal_completion"
+ *                                                                n_experts_per_device]
+ *   top_k                experts per token                      ["P3PeerSendConfig" top_k]
+ *   num_tokens           tokens per source rank in this batch (T)
+ *   max_tokens_per_rank  token capacity of each receive buffer (>= num_tokens)
+ *                                                               ["P3PeerSendConfig"]
+ *   K, N                 down-projection: rows of K inputs give rows of N outputs
+ *   msg_bytes            bytes of one received row; must equal 2*N (bf16 rows)
+ *   dtype                EP_BF16 or EP_FP8_1D2D
+ *   send_warps           warps reserved for the sink above the output warps
+ *                        ("EpiloguePeerSink" SendWarps): 0 runs the send inside the
+ *                        output warps; -1 lets the library choose.
+ */
+typedef struct {
+    int32_t n_ranks;
+    int32_t my_rank;
+    int32_t n_local_experts;
+    int32_t top_k;
+    int32_t num_tokens;
+    int32_t max_tokens_per_rank;
+    int32_t K;
+    int32_t N;
+    int32_t msg_bytes;
+    int32_t dtype;
+    int32_t send_warps;
+} ep_config;
+
+/* ------------------------------------------------------------------ plan */
+
+/*
+ * Receiving-side row plan of rank cfg->my_rank (the layout a dispatch step
+ * produces and the grouped GEMM consumes). Rows of local expert e are
+ * contiguous, ordered by source rank, then source token index, then top-k slot.
+ * All arrays are device memory owned by the caller:
+ *   expert_offsets [E_l+1]       first row of each local expert; [E_l] = row count
+ *   src_info       [max_rows][2] (src_idx, src_topk) of each row ["P3PeerSendConfig"
+ *                                src_info_ptr]
+ *   seg_offsets    [E_l][R+1]    first row of each (expert, source rank) segment
+ *   send_counts    [E_l][R]      rows of expert e from source rank rk: the count that
+ *                                ep_signal_completion publishes to rk
+ *   gather_idx     [max_rows]    flat routing index (rk*T + t)*top_k + j of each row
+ *   m_total        [1]           row count
+ *   status         [1]           EP_STATUS_* bits (OR-ed)
+ * max_rows is the capacity of src_info / gather_idx (and of the A operand).
+ */
+typedef struct {
+    int32_t *expert_offsets;
+    int32_t *src_info;
+    int32_t *seg_offsets;
+    int32_t *send_counts;
+    int32_t *gather_idx;
+    int32_t *m_total;
+    uint32_t *status;
+    int64_t max_rows;
+} ep_plan_out;
+
+/* Worst-case row count of one rank: num_tokens * n_ranks * min(top_k, E_l).
+ * Host only. Returns EP_OK or EP_ERR_INVALID_ARG. */
+int ep_plan_sizes(const ep_config *cfg, int64_t *max_rows);
+
+/*
+ * Build the plan of cfg->my_rank from topk_ids, a device array
+ * [n_ranks][num_tokens][top_k] of global expert ids. One small kernel; the
+ * result is deterministic. If the rows exceed out->max_rows the kernel sets
+ * EP_STATUS_CAPACITY and writes an empty plan (all offsets and counts 0).
+ */
+int ep_plan(const ep_config *cfg, const int32_t *topk_ids, const ep_plan_out *out,
+            ep_stream_t stream);
+
+/* -------------------------------------------- grouped GEMM + combine send */
+
+/*
+ * Runtime state of the fused send ("P3PeerSendConfig" fields, plus operands).
+ *   A                [max_rows][K] bf16 or e4m3, row-major, rows in plan order. Rows at
+ *                    or past the plan's row count are read (and ignored).
+ *   a_scales         EP_FP8_1D2D only: [max_rows][K/128] fp32
+ *   W                [E_l][N][K] bf16 or e4m3 (each expert's [N, K] weight, K contiguous)
+ *   w_scales         EP_FP8_1D2D only: [E_l][N/128][K/128] fp32
+ *   expert_offsets, src_info, seg_offsets, send_counts   the plan of my_rank (ep_plan)
+ *   max_rows         rows allocated for A (and src_info)
+ *   recv_buf_ptrs    [n_ranks] receive buffers, max_tokens_per_rank*top_k*msg_bytes bytes
+ *                    each. The row of (src_idx, src_topk) from the token-owning rank goes
+ *                    to byte (src_idx*top_k + src_topk)*msg_bytes + 2*n of that rank's
+ *                    buffer ("P3PeerSendConfig" recv_buf_layout).
+ *   recv_count_ptrs  [n_ranks] receive-count buffers, E_l*n_ranks + n_ranks uint64 words
+ *                    each: word e*n_ranks + rk holds the rows expert e of rank rk sent
+ *                    ("P3PeerSendConfig" recv_count_layout); word E_l*n_ranks + rk is
+ *                    rank rk's completion flag ("ep_signal_completion" rank_flag_offset,
+ *                    the buffer tail).
+ *   atomic_counter   [E_l] int32 tile-completion counters of my_rank's experts
+ *   rank_completion_counter  [n_ranks] int32 election counters, one per destination
+ *                    Both counter arrays must be zero before the first call; every
+ *                    call that completes without a status bit leaves them at zero.
+ *   epoch            value released into the rank flags; use a new value per call
+ *                    (e.g. 1, 2, 3, ...) so a consumer can tell calls apart.
+ *   p3_control       >= 0: the sink owns the output (no local C); < 0: the sink is
+ *                    disabled and rows go to the local C instead, with no signalling
+ *                    ("EpiloguePeerSink" p3_control: negative disables the sink).
+ *   C                [max_rows][N] bf16, used only when p3_control < 0.
+ *   status           device word for EP_STATUS_* bits.
+ *   trace            reserved: must be NULL.
+ *   timeout_ns       limit of each bounded wait inside the kernel (0: 2 s).
+ */
+typedef struct {
+    const void *A;
+    const float *a_scales;
+    const void *W;
+    const float *w_scales;
+    const int32_t *expert_offsets;
+    const int32_t *src_info;
+    const int32_t *seg_offsets;
+    const int32_t *send_counts;
+    int64_t max_rows;
+    uint8_t *recv_buf_ptrs[EP_MAX_RANKS];
+    uint64_t *recv_count_ptrs[EP_MAX_RANKS];
+    int32_t *atomic_counter;
+    int32_t *rank_completion_counter;
+    uint64_t epoch;
+    int32_t p3_control;
+    void *C;
+    uint32_t *status;
+    uint64_t *trace;
+    int64_t timeout_ns;
+} ep_send_args;
+
+/*
+ * One persistent kernel: for every local expert e and every 128-row tile of its
+ * rows and every column block, Y_e = A_e * W_e^T on the tensor cores (fp32
+ * accumulation), rounded to bf16 and written row by row to the receive buffer of
+ * the rank that owns each row's token. No local C tensor exists ("EpiloguePeerSink"
+ * Enabled: the local store and its TMA descriptor are dead).
+ * When the last tile of expert e is done, for every destination rank dst: a plain
+ * store of the count word, then an acquire-release increment of
+ * rank_completion_counter[dst]; the call that sees E_l-1 release-stores (system
+ * scope) `epoch` into dst's flag word for my_rank ("ep_signal_completion",
+ * ep_ord_r with has_rank_flag). Experts with no rows signal count 0.
+ */
+int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *args,
+                              ep_stream_t stream);
+
+/* --------------------------------------------------------------- combine */
+
+/*
+ * Gate-weighted combine on rank cfg->my_rank.
+ *   recv_buf    this rank's receive buffer (layout above)
+ *   recv_count  this rank's receive-count buffer (layout above)
+ *   gates       [num_tokens][top_k] fp32
+ *   out         [num_tokens][N] bf16: out[t][n] = bf16(sum_j gates[t][j] * row(t, j)[n])
+ *   epoch       the flag value to wait for from every source rank
+ *   timeout_ns  limit of the flag wait (0: 2 s); on expiry EP_STATUS_TIMEOUT is set
+ *               and the affected outputs are left unwritten
+ * Each thread block acquires every source rank's flag once (system scope) before
+ * reading the rows, as the fused consumer of "ep_signal_completion" does.
+ */
+typedef struct {
+    const uint8_t *recv_buf;
+    const uint64_t *recv_count;
+    const float *gates;
+    void *out;
+    uint64_t epoch;
+    int64_t timeout_ns;
+    uint32_t *status;
+} ep_combine_args;
+
+int ep_combine_reduce(const ep_config *cfg, const ep_combine_args *args, ep_stream_t stream);
+
+/* Static description of a return code or status bit set. */
+const char *ep_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_EP_H */

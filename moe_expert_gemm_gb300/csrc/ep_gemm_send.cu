@@ -1,0 +1,424 @@
+// Grouped expert GEMM with the EP-combine send fused into its epilogue.
+//
+// "EpiloguePeerSink" (Modular MAX Mojo API, sm100_structured output_writer): the
+// epilogue hands its finished output tile to a sink instead of storing it to the
+// local C; with the sink enabled the local store and its TMA descriptor do not
+// exist. "P3PeerSendConfig": each valid row m of a tile (m < m_end) goes to the
+// receive buffer of the rank owning its token, at
+// (src_idx*top_k + src_topk)*msg_bytes + byte_off. "ep_signal_completion"
+// (shmem/ep_comm, ep_ord_r with has_rank_flag): per-expert count words are plain
+// stores made before an acquire-release election on a per-destination counter;
+// the producer elected last release-stores the rank flag.
+//
+// Design for sm_103a: one persistent CTA per SM walks a static schedule of
+// (expert, 128-row block, BN-column block) tiles. Warp 0 issues TMA loads of A and
+// W into a STAGES-deep ring of 128-byte-swizzled shared-memory tiles; warp 1
+// allocates TMEM and issues tcgen05.mma (M=128, N=BN, K=16 per instruction) into
+// one of two TMEM accumulators; warps 2-5 (one per TMEM lane quarter) drain an
+// accumulator with tcgen05.ld, round to bf16, stage 32 rows x 64 columns per warp
+// in shared memory and write each row's 128 contiguous bytes to its destination
+// with 16-byte stores (8 lanes per row). The double-buffered accumulator lets the
+// MMA of tile i+1 run while tile i is being sent. After the last row of a tile a
+// named barrier and one acquire-release increment count the tile; the CTA that
+// completes an expert's last tile runs the completion signalling.
+//
+// Every wait is bounded (timeout_ns of %globaltimer): on expiry the kernel sets
+// EP_STATUS_TIMEOUT, the other roles stop at their next wait, outstanding TMA
+// loads and MMAs are waited for (again bounded), TMEM is freed and the CTA exits.
+#include <cuda_bf16.h>
+
+#include "ep_internal.h"
+#include "ep_ptx.cuh"
+
+namespace ep {
+
+template <int BN, int STAGES>
+struct GemmLayout {
+    static constexpr int kABytes = BM * kRowBytesK;
+    static constexpr int kBBytes = BN * kRowBytesK;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kEpiWarps = 4;
+    static constexpr int kWarpStaging = 32 * 128;  // 32 rows x 64 bf16 columns
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + STAGES * kABytes;
+    static constexpr int kOffStaging = kOffB + STAGES * kBBytes;
+    static constexpr int kOffBars = kOffStaging + kEpiWarps * kWarpStaging;
+    static constexpr int kNumBars = 2 * STAGES + 5;  // full, empty, acc_full x2, acc_empty x2, mma_done
+    static constexpr int kOffTmemSlot = kOffBars + kNumBars * 8;
+    static constexpr int kOffAbort = kOffTmemSlot + 4;
+    static constexpr int kOffPtrs = (kOffAbort + 4 + 15) / 16 * 16;  // 8 recv_buf + 8 recv_count
+    static constexpr int kOffTileStart = kOffPtrs + 16 * 8;
+    static constexpr int kOffExpertOff = kOffTileStart + 4 * (EP_MAX_LOCAL_EXPERTS + 1);
+    static constexpr int kEnd = kOffExpertOff + 4 * (EP_MAX_LOCAL_EXPERTS + 1);
+    static constexpr int kSmemBytes = kEnd + 1024;  // slack to align the base to 1024
+    static constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators
+    static constexpr int kThreads = 192;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM columns");
+};
+
+__device__ __forceinline__ void raise_abort(uint32_t *status, volatile int *abort_flag)
+{
+    atomicOr(status, EP_STATUS_TIMEOUT);
+    *abort_flag = 1;
+}
+
+// Completion signalling of local expert e towards every destination rank.
+__device__ void signal_expert(const SendParams &p, int e, uint64_t *const *cnt)
+{
+    const int R = p.n_ranks;
+    for (int dst = 0; dst < R; ++dst) {
+        uint64_t *words = cnt[dst];
+        // plain progress store of the count word, recv_count_layout((e, my_rank))
+        volatile uint64_t *w = words + static_cast<int64_t>(e) * R + p.my_rank;
+        *w = static_cast<uint64_t>(p.send_counts[e * R + dst]);
+        // election: releases this producer's payload and count, acquires its predecessors'
+        const int old = atom_add_acq_rel_sys(&p.rank_counter[dst], 1);
+        if (old == p.El - 1) {
+            // last expert of this rank for dst: re-arm the counter for the next call and
+            // publish the whole rank with one system-scope release of the rank flag
+            *reinterpret_cast<volatile int *>(&p.rank_counter[dst]) = 0;
+            st_release_sys_u64(words + static_cast<int64_t>(p.El) * R + p.my_rank, p.epoch);
+        }
+    }
+}
+
+struct TileCoord {
+    int e, m_abs, m_end, nb;
+};
+
+__device__ __forceinline__ TileCoord decode_tile(int t, const int *tile_start, const int *eoff,
+                                                 int El, int n_blocks)
+{
+    // the largest expert whose first tile is <= t owns t (empty experts share starts)
+    int lo = 0, hi = El - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tile_start[mid] <= t)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    TileCoord c;
+    c.e = lo;
+    const int local = t - tile_start[lo];
+    const int mt = local / n_blocks;
+    c.nb = local - mt * n_blocks;
+    c.m_abs = eoff[lo] + mt * BM;
+    c.m_end = eoff[lo + 1];
+    return c;
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    gemm_send_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                          const __grid_constant__ CUtensorMap tmap_b,
+                          const __grid_constant__ SendParams p)
+{
+    using L = GemmLayout<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBars);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES;
+    uint64_t *acc_full = bars + 2 * STAGES;
+    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *mma_done = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffTmemSlot);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffAbort);
+    uint8_t **s_recv = reinterpret_cast<uint8_t **>(smem + L::kOffPtrs);
+    uint64_t **s_cnt = reinterpret_cast<uint64_t **>(smem + L::kOffPtrs + 64);
+    int *s_tile_start = reinterpret_cast<int *>(smem + L::kOffTileStart);
+    int *s_eoff = reinterpret_cast<int *>(smem + L::kOffExpertOff);
+    const int El = p.El;
+
+    // ---------------------------------------------------------------- prologue
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], L::kEpiWarps);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (threadIdx.x < EP_MAX_RANKS) {
+        s_recv[threadIdx.x] = p.recv_buf[threadIdx.x];
+        s_cnt[threadIdx.x] = p.recv_count[threadIdx.x];
+    }
+    if (threadIdx.x == 32) {
+        // expert row ranges, made monotone and clamped to the rows of A so that a
+        // malformed plan cannot send reads past the plan arrays
+        int prev = 0;
+        for (int e = 0; e <= El; ++e) {
+            int v = p.expert_offsets[e];
+            v = v < prev ? prev : v;
+            v = v > p.max_rows ? static_cast<int>(p.max_rows) : v;
+            s_eoff[e] = v;
+            prev = v;
+        }
+        int acc = 0;
+        for (int e = 0; e < El; ++e) {
+            s_tile_start[e] = acc;
+            acc += (s_eoff[e + 1] - s_eoff[e] + BM - 1) / BM * p.n_blocks;
+        }
+        s_tile_start[El] = acc;
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tmem_alloc(tmem_slot, L::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmap_a);
+        tma_prefetch_map(&tmap_b);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total_tiles = s_tile_start[El];
+
+    if (warp == 0) {
+        // ------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t used_mask = 0, last_parity = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+                const TileCoord c = decode_tile(t, s_tile_start, s_eoff, El, p.n_blocks);
+                const int w_row = c.e * p.N + c.nb * BN;
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
+                    tma_load_2d(smem + L::kOffA + stage * L::kABytes, &tmap_a, &full[stage],
+                                kb * 64, c.m_abs);
+                    tma_load_2d(smem + L::kOffB + stage * L::kBBytes, &tmap_b, &full[stage],
+                                kb * 64, w_row);
+                    used_mask |= 1u << stage;
+                    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok)
+                raise_abort(p.status, abort_flag);
+            // loads complete whether or not anyone consumes them: wait for the last
+            // one of every stage before the block may exit
+            volatile int no_abort = 0;
+            for (int s = 0; s < STAGES; ++s)
+                if (used_mask & (1u << s))
+                    mbar_wait(&full[s], (last_parity >> s) & 1u, p.timeout_ns, &no_abort);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ----------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(1u, BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int i = 0;
+            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++i) {
+                const int as = i & 1;
+                const uint32_t aphase = (i >> 1) & 1;
+                if (!mbar_wait(&acc_empty[as], aphase ^ 1u, p.timeout_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as * BN);
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + L::kOffA + stage * L::kABytes);
+                    const uint32_t b_addr = smem_u32(smem + L::kOffB + stage * L::kBBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f16(d_tmem, desc_kmajor_sw128(a_addr + kk * 32),
+                                desc_kmajor_sw128(b_addr + kk * 32), idesc,
+                                (kb | kk) != 0 ? 1u : 0u);
+                    mma_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                mma_commit(&acc_full[as]);
+            }
+            if (!ok)
+                raise_abort(p.status, abort_flag);
+            // every MMA issued so far has finished once this commit lands
+            mma_commit(mma_done);
+            volatile int no_abort = 0;
+            mbar_wait(mma_done, 0, p.timeout_ns, &no_abort);
+        }
+        __syncwarp();
+    } else {
+        // --------------------------------------------------- epilogue + sink
+        const int q = warp & 3;  // TMEM lane quarter this warp may read
+        const int epi_tid = threadIdx.x - 64;
+        const uint32_t stg = smem_u32(smem + L::kOffStaging + (warp - 2) * L::kWarpStaging);
+        const int R = p.n_ranks;
+
+        if (p.sink_enabled && blockIdx.x == 0 && epi_tid == 0) {
+            // experts without rows have no tile to complete: signal their zero counts now
+            for (int e = 0; e < El; ++e)
+                if (s_eoff[e + 1] == s_eoff[e])
+                    signal_expert(p, e, s_cnt);
+        }
+
+        bool ok = true;
+        int i = 0;
+        for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++i) {
+            const TileCoord c = decode_tile(t, s_tile_start, s_eoff, El, p.n_blocks);
+            const int as = i & 1;
+            const uint32_t aphase = (i >> 1) & 1;
+
+            // resolve this thread's row destination while the MMA runs
+            const int m = c.m_abs + q * 32 + lane;
+            uint8_t *row_base = nullptr;
+            if (m < c.m_end) {
+                if (p.sink_enabled) {
+                    const int *seg = p.seg_offsets + c.e * (R + 1);
+                    int dst = -1;
+                    for (int rk = 0; rk < R; ++rk)
+                        if (m >= __ldg(seg + rk) && m < __ldg(seg + rk + 1))
+                            dst = rk;
+                    const int2 si = __ldg(reinterpret_cast<const int2 *>(p.src_info) + m);
+                    if (dst < 0 || si.x < 0 || si.x >= p.max_tokens || si.y < 0 ||
+                        si.y >= p.top_k) {
+                        atomicOr(p.status, EP_STATUS_BOUNDS);
+                    } else {
+                        row_base = s_recv[dst] +
+                                   (static_cast<int64_t>(si.x) * p.top_k + si.y) * p.msg_bytes;
+                    }
+                } else {
+                    row_base = p.C + static_cast<int64_t>(m) * p.N * 2;
+                }
+            }
+
+            ok = mbar_wait(&acc_full[as], aphase, p.timeout_ns, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok)
+                break;
+            tc_fence_after();
+
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(as * BN);
+#pragma unroll 1
+            for (int sub = 0; sub < BN / 64; ++sub) {
+                uint32_t v0[32], v1[32];
+                tmem_ld_32x32b_x32(t_row + sub * 64, v0);
+                tmem_ld_32x32b_x32(t_row + sub * 64 + 32, v1);
+                tmem_ld_wait();
+                // fp32 -> bf16 (nearest even), this thread's row, 8 chunks of 16 bytes
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint32_t *v = ch < 4 ? v0 + ch * 8 : v1 + (ch - 4) * 8;
+                    uint32_t w[4];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        __nv_bfloat162 b = __float22bfloat162_rn(
+                            make_float2(__uint_as_float(v[2 * h]), __uint_as_float(v[2 * h + 1])));
+                        w[h] = *reinterpret_cast<uint32_t *>(&b);
+                    }
+                    st_shared_v4(stg + lane * 128 + ((ch ^ (lane & 7)) << 4),
+                                 make_uint4(w[0], w[1], w[2], w[3]));
+                }
+                __syncwarp();
+                // 8 lanes per row: each row's 128 bytes leave as one contiguous segment
+                const int col_byte = (c.nb * BN + sub * 64) * 2;
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int row = it * 4 + (lane >> 3);
+                    const int ch = lane & 7;
+                    const unsigned long long base = __shfl_sync(
+                        0xffffffffu, reinterpret_cast<unsigned long long>(row_base), row);
+                    const uint4 val = ld_shared_v4(stg + row * 128 + ((ch ^ (row & 7)) << 4));
+                    if (base != 0ull)
+                        st_global_v4(reinterpret_cast<uint8_t *>(base) + col_byte + ch * 16, val);
+                }
+                __syncwarp();
+            }
+            // accumulator drained: hand it back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&acc_empty[as]);
+
+            if (p.sink_enabled) {
+                // all 128 sink threads' stores of this tile precede the count increment
+                named_bar_sync(1, 128);
+                if (epi_tid == 0) {
+                    const int tiles_e =
+                        (c.m_end - s_eoff[c.e] + BM - 1) / BM * p.n_blocks;
+                    const int old = atom_add_acq_rel_gpu(&p.atomic_counter[c.e], 1);
+                    if (old == tiles_e - 1) {
+                        *reinterpret_cast<volatile int *>(&p.atomic_counter[c.e]) = 0;
+                        signal_expert(p, c.e, s_cnt);
+                    }
+                }
+            }
+        }
+        if (!ok && lane == 0)
+            raise_abort(p.status, abort_flag);
+    }
+
+    // --------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, L::kTmemCols);
+    }
+}
+
+template <int BN, int STAGES>
+static cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const SendParams &p,
+                             int grid, cudaStream_t s)
+{
+    using L = GemmLayout<BN, STAGES>;
+    auto kern = gemm_send_bf16_kernel<BN, STAGES>;
+    cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+    if (err != cudaSuccess)
+        return err;
+    kern<<<grid, L::kThreads, L::kSmemBytes, s>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_send_bf16(const CUtensorMap &ta, const CUtensorMap &tb,
+                                  const SendParams &p, int bn, int grid, cudaStream_t s)
+{
+    switch (bn) {
+    case 256:
+        return launch_bn<256, 4>(ta, tb, p, grid, s);
+    case 128:
+        return launch_bn<128, 6>(ta, tb, p, grid, s);
+    case 64:
+        return launch_bn<64, 8>(ta, tb, p, grid, s);
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace ep

@@ -1,0 +1,66 @@
+// Launch-side definitions shared by the host API and the kernels.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (type only; the encoder comes from the runtime's driver entry point)
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "moe_ep.h"
+
+namespace ep {
+
+constexpr int BM = 128;          // rows per tile (tcgen05 M, one TMEM lane per row)
+constexpr int kRowBytesK = 128;  // bytes of K per stage and row: one 128-byte swizzle atom
+
+// Everything the fused GEMM + send kernel reads besides the two tensor maps.
+struct SendParams {
+    int n_ranks, my_rank, El, top_k, K, N, max_tokens;
+    int n_blocks;      // column blocks per expert (N / BN)
+    int num_k_blocks;  // K / (elements per 128 bytes)
+    int64_t msg_bytes;
+    int64_t max_rows;
+    const int32_t *expert_offsets;
+    const int32_t *src_info;
+    const int32_t *seg_offsets;
+    const int32_t *send_counts;
+    uint8_t *recv_buf[EP_MAX_RANKS];
+    uint64_t *recv_count[EP_MAX_RANKS];
+    int32_t *atomic_counter;
+    int32_t *rank_counter;
+    uint64_t epoch;
+    int sink_enabled;  // p3_control >= 0
+    uint8_t *C;        // local output when the sink is disabled
+    uint32_t *status;
+    uint64_t timeout_ns;
+    const float *a_scales;
+    const float *w_scales;
+};
+
+struct PlanParams {
+    int n_ranks, my_rank, El, top_k, T;
+    int64_t max_rows;
+    const int32_t *topk_ids;
+    int32_t *expert_offsets, *src_info, *seg_offsets, *send_counts, *gather_idx, *m_total;
+    uint32_t *status;
+};
+
+struct CombineParams {
+    int n_ranks, El, top_k, T, N;
+    int64_t msg_bytes;
+    const uint8_t *recv_buf;
+    const uint64_t *recv_count;
+    const float *gates;
+    uint8_t *out;
+    uint64_t epoch;
+    uint64_t timeout_ns;
+    uint32_t *status;
+};
+
+// Kernel launchers; each returns the launch's cudaError_t.
+cudaError_t launch_plan(const PlanParams &p, cudaStream_t s);
+cudaError_t launch_gemm_send_bf16(const CUtensorMap &ta, const CUtensorMap &tb,
+                                  const SendParams &p, int bn, int grid, cudaStream_t s);
+cudaError_t launch_combine(const CombineParams &p, int num_sms, cudaStream_t s);
+
+}  // namespace ep

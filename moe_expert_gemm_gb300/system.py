@@ -1,0 +1,170 @@
+"""Device state of a set of logical EP ranks on one GPU, driven through the C ABI.
+
+PyTorch only allocates device memory and provides streams; every step runs in
+``libmoe_ep.so``. On one GPU the receive buffers of the other logical ranks
+are separate allocations in the same HBM that stand in for peer memory, so a
+producer call for rank r writes into every rank's buffer exactly as it would
+over direct peer stores.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (EP_BF16, EP_FP8_1D2D, ep_combine_args, ep_combine_reduce, ep_config, ep_plan,
+               ep_plan_out, ep_plan_sizes, ep_send_args, grouped_gemm_combine_send, ptr)
+
+SENTINEL_BYTE = 0xFF  # received bf16 0xFFFF is a NaN: an unwritten slot cannot pass
+STATUS_PLAN, STATUS_SEND, STATUS_COMBINE = 0, 1, 2
+
+
+class EpSystem:
+    def __init__(self, n_ranks: int, n_local_experts: int, top_k: int, tokens: int, K: int,
+                 N: int, dtype: str = "bf16", device="cuda", max_tokens: int | None = None,
+                 timeout_ns: int = 0, send_warps: int = -1):
+        self.R, self.El, self.k, self.T, self.K, self.N = (n_ranks, n_local_experts, top_k,
+                                                           tokens, K, N)
+        self.dtype = dtype
+        self.dt_code = {"bf16": EP_BF16, "fp8_1d2d": EP_FP8_1D2D}[dtype]
+        self.device = torch.device(device)
+        self.max_tokens = tokens if max_tokens is None else max_tokens
+        self.msg_bytes = 2 * N
+        self.timeout_ns = timeout_ns
+        self.send_warps = send_warps
+        dev = self.device
+        R, El = self.R, self.El
+        self.recv = [torch.full((self.max_tokens * top_k * self.msg_bytes,), SENTINEL_BYTE,
+                                dtype=torch.uint8, device=dev) for _ in range(R)]
+        self.counts = [torch.full((El * R + R,), -1, dtype=torch.int64, device=dev)
+                       for _ in range(R)]
+        self.atomic_counter = [torch.zeros(El, dtype=torch.int32, device=dev) for _ in range(R)]
+        self.rank_counter = [torch.zeros(R, dtype=torch.int32, device=dev) for _ in range(R)]
+        self.status = torch.zeros(8, dtype=torch.int32, device=dev)
+        self.topk = None
+        self.plans: list[dict | None] = [None] * R
+        self.ops: list[dict | None] = [None] * R
+        self.gates: list[torch.Tensor | None] = [None] * R
+        self.out: list[torch.Tensor | None] = [None] * R
+
+    # ------------------------------------------------------------- set-up
+    def cfg(self, rank: int) -> ep_config:
+        return ep_config(self.R, rank, self.El, self.k, self.T, self.max_tokens, self.K, self.N,
+                         self.msg_bytes, self.dt_code, self.send_warps)
+
+    def reset_buffers(self):
+        for b in self.recv:
+            b.fill_(SENTINEL_BYTE)
+        for c in self.counts:
+            c.fill_(-1)
+
+    def set_routing(self, topk_ids):
+        t = torch.as_tensor(np.ascontiguousarray(topk_ids, dtype=np.int32))
+        assert tuple(t.shape) == (self.R, self.T, self.k)
+        self.topk = t.to(self.device)
+
+    def plan(self, rank: int, stream=None, max_rows: int | None = None) -> dict:
+        cap = ep_plan_sizes(self.cfg(rank)) if max_rows is None else max_rows
+        dev, El, R = self.device, self.El, self.R
+        p = dict(expert_offsets=torch.zeros(El + 1, dtype=torch.int32, device=dev),
+                 src_info=torch.zeros((max(cap, 1), 2), dtype=torch.int32, device=dev),
+                 seg_offsets=torch.zeros((El, R + 1), dtype=torch.int32, device=dev),
+                 send_counts=torch.zeros((El, R), dtype=torch.int32, device=dev),
+                 gather_idx=torch.zeros(max(cap, 1), dtype=torch.int32, device=dev),
+                 m_total=torch.zeros(1, dtype=torch.int32, device=dev), capacity=cap)
+        out = ep_plan_out(ptr(p["expert_offsets"]), ptr(p["src_info"]), ptr(p["seg_offsets"]),
+                          ptr(p["send_counts"]), ptr(p["gather_idx"]), ptr(p["m_total"]),
+                          self.status.data_ptr() + 4 * STATUS_PLAN, cap)
+        ep_plan(self.cfg(rank), self.topk, out, stream)
+        self.plans[rank] = p
+        return p
+
+    def set_operands(self, rank: int, A: np.ndarray, W: np.ndarray, a_scales=None,
+                     w_scales=None, pad_rows: int = 0):
+        """Upload a rank's operands (bf16 as uint16 bit patterns, e4m3 as uint8).
+        ``pad_rows`` extra rows are appended to A (they are read by tiles that run
+        past the last row and never sent)."""
+        dev = self.device
+        rows = max(A.shape[0] + pad_rows, 1)
+        if self.dtype == "bf16":
+            a = torch.zeros((rows, self.K), dtype=torch.int16)
+            a[:A.shape[0]] = torch.from_numpy(np.ascontiguousarray(A).view(np.int16))
+            w = torch.from_numpy(np.ascontiguousarray(W).view(np.int16))
+            ops = dict(A=a.view(torch.bfloat16).to(dev), W=w.view(torch.bfloat16).to(dev))
+        else:
+            a = torch.zeros((rows, self.K), dtype=torch.uint8)
+            a[:A.shape[0]] = torch.from_numpy(np.ascontiguousarray(A))
+            sa = torch.zeros((rows, self.K // 128), dtype=torch.float32)
+            sa[:A.shape[0]] = torch.from_numpy(np.ascontiguousarray(a_scales, dtype=np.float32))
+            ops = dict(A=a.to(dev), W=torch.from_numpy(np.ascontiguousarray(W)).to(dev),
+                       a_scales=sa.to(dev),
+                       w_scales=torch.from_numpy(np.ascontiguousarray(w_scales,
+                                                                      dtype=np.float32)).to(dev))
+        self.ops[rank] = ops
+        return ops
+
+    def set_gates(self, rank: int, gates: np.ndarray):
+        self.gates[rank] = torch.from_numpy(np.ascontiguousarray(gates, dtype=np.float32)).to(
+            self.device)
+        self.out[rank] = torch.zeros((self.T, self.N), dtype=torch.bfloat16, device=self.device)
+
+    # ---------------------------------------------------------------- calls
+    def send_args(self, rank: int, epoch: int, p3_control: int = 0, C=None) -> ep_send_args:
+        p, o = self.plans[rank], self.ops[rank]
+        a = ep_send_args()
+        a.A = ptr(o["A"])
+        a.a_scales = ptr(o.get("a_scales"))
+        a.W = ptr(o["W"])
+        a.w_scales = ptr(o.get("w_scales"))
+        a.expert_offsets = ptr(p["expert_offsets"])
+        a.src_info = ptr(p["src_info"])
+        a.seg_offsets = ptr(p["seg_offsets"])
+        a.send_counts = ptr(p["send_counts"])
+        a.max_rows = min(int(o["A"].shape[0]), int(p["src_info"].shape[0]))
+        for d in range(self.R):
+            a.recv_buf_ptrs[d] = ptr(self.recv[d])
+            a.recv_count_ptrs[d] = ptr(self.counts[d])
+        a.atomic_counter = ptr(self.atomic_counter[rank])
+        a.rank_completion_counter = ptr(self.rank_counter[rank])
+        a.epoch = epoch
+        a.p3_control = p3_control
+        a.C = ptr(C)
+        a.status = self.status.data_ptr() + 4 * STATUS_SEND
+        a.trace = None
+        a.timeout_ns = self.timeout_ns
+        return a
+
+    def send(self, rank: int, epoch: int, stream=None, p3_control: int = 0, C=None):
+        grouped_gemm_combine_send(self.cfg(rank), self.send_args(rank, epoch, p3_control, C),
+                                  stream)
+
+    def combine_args(self, rank: int, epoch: int, gates=None, out=None) -> ep_combine_args:
+        g = self.gates[rank] if gates is None else gates
+        o = self.out[rank] if out is None else out
+        return ep_combine_args(ptr(self.recv[rank]), ptr(self.counts[rank]), ptr(g), ptr(o),
+                               epoch, self.timeout_ns,
+                               self.status.data_ptr() + 4 * STATUS_COMBINE)
+
+    def combine(self, rank: int, epoch: int, stream=None, gates=None, out=None):
+        ep_combine_reduce(self.cfg(rank), self.combine_args(rank, epoch, gates, out), stream)
+
+    def publish_peer_flags(self, rank: int, epoch: int):
+        """Stand-in for the other ranks finishing on their own GPUs: write the flag
+        words of every source rank except ``rank`` in ``rank``'s count buffer."""
+        base = self.El * self.R
+        idx = [base + q for q in range(self.R) if q != rank]
+        if idx:
+            self.counts[rank][idx] = epoch
+
+    # -------------------------------------------------------------- readback
+    def status_words(self) -> np.ndarray:
+        return self.status.cpu().numpy().view(np.uint32)
+
+    def plan_host(self, rank: int) -> dict:
+        p = self.plans[rank]
+        m = int(p["m_total"].item())
+        return dict(expert_offsets=p["expert_offsets"].cpu().numpy(),
+                    src_info=p["src_info"][:m].cpu().numpy(),
+                    seg_offsets=p["seg_offsets"].cpu().numpy(),
+                    send_counts=p["send_counts"].cpu().numpy(),
+                    gather_idx=p["gather_idx"][:m].cpu().numpy(), m_total=m)

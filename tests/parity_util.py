@@ -1,0 +1,69 @@
+"""Shared helpers of the GPU parity tests: build the logical ranks on the GPU from
+seeded inputs, run the path through the C ABI, and compare with the oracle.
+
+Tolerance (values): max_i |g_i - r_i| / max(|r_i|, rms(r)) <= 1e-2 for bf16
+operands and 3e-2 for blockwise fp8 -- the relative error bound of the stated
+target, floored at the rms so that cancellation points near zero do not count
+as failures. Indices, counts and flags are compared bit for bit.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+TOL = {"bf16": 1e-2, "fp8_1d2d": 3e-2}
+
+
+def bf16_to_f32(bits) -> np.ndarray:
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def max_rel_err(got_bits, ref_bits) -> float:
+    g = bf16_to_f32(got_bits).astype(np.float64)
+    r = bf16_to_f32(ref_bits).astype(np.float64)
+    if g.size == 0:
+        return 0.0
+    if np.isnan(g).any():
+        return float("inf")
+    rms = np.sqrt(np.mean(r * r))
+    den = np.maximum(np.abs(r), max(rms, 1e-30))
+    return float(np.max(np.abs(g - r) / den))
+
+
+def make_inputs(w, routing=None):
+    from synth import make_rank_values, make_routing, rows_per_rank
+    routing = make_routing(w) if routing is None else routing
+    rows = rows_per_rank(w, routing.topk_ids)
+    values = [make_rank_values(w, r, int(rows[r])) for r in range(w.n_ranks)]
+    return routing, values
+
+
+def build_system(w, routing, values, timeout_ns=0, send_warps=-1):
+    from moe_expert_gemm_gb300.system import EpSystem
+    s = EpSystem(w.n_ranks, w.n_local_experts, w.top_k, w.tokens, w.K, w.N, w.dtype,
+                 timeout_ns=timeout_ns, send_warps=send_warps)
+    s.set_routing(routing.topk_ids)
+    for r in range(w.n_ranks):
+        s.plan(r)
+        v = values[r]
+        s.set_operands(r, v["A"], v["W"], v.get("a_scales"), v.get("w_scales"))
+        s.set_gates(r, routing.gates[r])
+    return s
+
+
+def run_all(s, epoch: int):
+    """Every producer, then every destination's combine, on the current stream."""
+    for r in range(s.R):
+        s.send(r, epoch)
+    for d in range(s.R):
+        s.combine(d, epoch)
+
+
+def assert_plan_equal(got: dict, want) -> None:
+    assert got["m_total"] == want.m_total
+    np.testing.assert_array_equal(got["expert_offsets"], want.expert_offsets)
+    np.testing.assert_array_equal(got["src_info"], want.src_info)
+    np.testing.assert_array_equal(got["seg_offsets"], want.seg_offsets)
+    np.testing.assert_array_equal(got["send_counts"], want.send_counts)
+    np.testing.assert_array_equal(got["gather_idx"], want.gather_idx)

@@ -1,0 +1,97 @@
+"""The C-ABI library builds for sm_103a, loads, exports every entry point the
+header declares, and rejects bad arguments on the host (no GPU needed: argument
+checks run before any CUDA call)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_expert_gemm_gb300 as ep
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_ep.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\([^;{]*\)\s*;", text, flags=re.M)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ep.build()
+    return ep.load()
+
+
+def test_header_declares_the_entry_points():
+    assert set(declared_functions()) >= set(ep.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def _cfg(**kw):
+    base = dict(n_ranks=4, my_rank=0, n_local_experts=2, top_k=2, num_tokens=64,
+                max_tokens_per_rank=64, K=256, N=128, msg_bytes=256, dtype=ep.EP_BF16,
+                send_warps=-1)
+    base.update(kw)
+    return ep.ep_config(**base)
+
+
+def test_plan_sizes(lib):
+    assert ep.ep_plan_sizes(_cfg()) == 64 * 4 * 2
+    assert ep.ep_plan_sizes(_cfg(n_local_experts=1, n_ranks=8)) == 64 * 8 * 1
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_ranks=9, my_rank=0), ep.EP_ERR_UNSUPPORTED),  # reach of direct stores is 8 ranks
+    (dict(my_rank=4), ep.EP_ERR_INVALID_ARG),
+    (dict(msg_bytes=250), ep.EP_ERR_INVALID_ARG),
+    (dict(num_tokens=65), ep.EP_ERR_INVALID_ARG),
+    (dict(top_k=9), ep.EP_ERR_INVALID_ARG),
+    (dict(n_local_experts=300, top_k=2), ep.EP_ERR_UNSUPPORTED),
+    (dict(dtype=7), ep.EP_ERR_INVALID_ARG),
+    (dict(send_warps=3), ep.EP_ERR_INVALID_ARG),
+])
+def test_bad_config_rejected_before_launch(lib, kw, code):
+    cfg = _cfg(**kw)
+    out = ctypes.c_int64(0)
+    assert lib.ep_plan_sizes(ctypes.byref(cfg), ctypes.byref(out)) == code
+    args = ep.ep_send_args()
+    assert lib.grouped_gemm_combine_send(ctypes.byref(cfg), ctypes.byref(args), None) == code
+    cargs = ep.ep_combine_args()
+    assert lib.ep_combine_reduce(ctypes.byref(cfg), ctypes.byref(cargs), None) == code
+
+
+def test_zero_args_are_rejected(lib):
+    """Zero-initialised send arguments (every pointer NULL) never launch."""
+    cfg = _cfg()
+    assert lib.grouped_gemm_combine_send(ctypes.byref(cfg), ctypes.byref(ep.ep_send_args()),
+                                         None) == ep.EP_ERR_INVALID_ARG
+    assert lib.ep_plan(ctypes.byref(cfg), None, ctypes.byref(ep.ep_plan_out()),
+                       None) == ep.EP_ERR_INVALID_ARG
+
+
+def test_unaligned_operand_rejected(lib):
+    cfg = _cfg()
+    a = ep.ep_send_args()
+    a.A, a.W = 0x1000008, 0x2000000
+    a.expert_offsets = a.src_info = a.seg_offsets = a.send_counts = a.status = 0x3000000
+    a.max_rows = 8
+    for r in range(4):
+        a.recv_buf_ptrs[r] = 0x4000000 + r * 0x100000
+        a.recv_count_ptrs[r] = 0x5000000 + r * 0x100000
+    a.atomic_counter = a.rank_completion_counter = 0x6000000
+    assert lib.grouped_gemm_combine_send(ctypes.byref(cfg), ctypes.byref(a), None) == \
+        ep.EP_ERR_INVALID_ARG
+
+
+def test_strerror(lib):
+    assert ep.ep_strerror(ep.EP_ERR_UNSUPPORTED) == "unsupported configuration"
+    assert "timed out" in ep.ep_strerror(ep.EP_STATUS_TIMEOUT)

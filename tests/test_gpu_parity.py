@@ -1,0 +1,148 @@
+"""Parity of the CUDA path with the oracle, through the C ABI (GPU).
+
+Small workloads run the oracle in full and are compared element by element:
+plans, every count and flag word bit for bit; every received row and every
+combined output within the tolerance; every receive slot written (the
+sentinel NaN would fail the value check).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.pipeline import full_pipeline
+from parity_util import (TOL, assert_plan_equal, build_system, make_inputs, max_rel_err,
+                         run_all)
+from synth import Routing, Workload, WORKLOADS, make_routing
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_full(w, routing=None, values=None, epoch=3):
+    routing, values = (routing, values) if values is not None else make_inputs(w, routing)
+    s = build_system(w, routing, values)
+    run_all(s, epoch)
+    torch.cuda.synchronize()
+    st = s.status_words()
+    assert (st == 0).all(), st
+    ref = full_pipeline(w, routing, values, epoch=epoch)
+    tol = TOL[w.dtype]
+    for r in range(w.n_ranks):
+        assert_plan_equal(s.plan_host(r), ref["plans"][r])
+    for d in range(w.n_ranks):
+        np.testing.assert_array_equal(s.counts[d].cpu().numpy().view(np.uint64), ref["counts"][d])
+        got = s.recv[d].cpu().numpy().view(np.uint16)
+        want = ref["recv"][d].view(np.uint16)
+        assert max_rel_err(got, want) <= tol, d
+        out = s.out[d].view(torch.int16).cpu().numpy().view(np.uint16)
+        assert max_rel_err(out, ref["out"][d]) <= tol, d
+    for r in range(w.n_ranks):  # counters re-armed for the next call
+        assert int(s.atomic_counter[r].abs().sum()) == 0
+        assert int(s.rank_counter[r].abs().sum()) == 0
+    return s, ref, routing, values
+
+
+def test_tiny_full_parity():
+    _check_full(WORKLOADS["tiny"])
+
+
+def test_tiny_two_epochs_in_a_row():
+    w = WORKLOADS["tiny"]
+    s, ref, routing, values = _check_full(w, epoch=1)
+    run_all(s, 2)
+    torch.cuda.synchronize()
+    assert (s.status_words() == 0).all()
+    ref2 = full_pipeline(w, routing, values, epoch=2)
+    for d in range(w.n_ranks):
+        np.testing.assert_array_equal(s.counts[d].cpu().numpy().view(np.uint64), ref2["counts"][d])
+        out = s.out[d].view(torch.int16).cpu().numpy().view(np.uint16)
+        assert max_rel_err(out, ref2["out"][d]) <= TOL[w.dtype]
+
+
+def _fixed_routing(w, ids, seed=5):
+    rng = np.random.default_rng(seed)
+    g = rng.random(ids.shape).astype(np.float32) + 0.1
+    return Routing(np.ascontiguousarray(ids, dtype=np.int32), (g / g.sum(-1, keepdims=True)))
+
+
+EDGE = [
+    # ragged tails around the 128-row tile: every token of every rank to experts 2 and 3
+    ("hot_pair_ragged", Workload("hot_pair", 4, 2, 2, 100, 256, 256, "bf16", "uniform",
+                                 "softmax_sel", 40), "hot"),
+    ("one_row_expert", Workload("one_row", 2, 2, 1, 1, 128, 128, "bf16", "uniform",
+                                "softmax_sel", 41), "random"),
+    ("bm_minus_one", Workload("bm_m1", 1, 1, 1, 127, 128, 128, "bf16", "uniform",
+                              "softmax_sel", 42), "random"),
+    ("bm_plus_one", Workload("bm_p1", 1, 1, 1, 129, 128, 128, "bf16", "uniform",
+                             "softmax_sel", 43), "random"),
+    ("single_rank_topk1", Workload("r1", 1, 3, 1, 77, 192, 192, "bf16", "uniform",
+                                   "softmax_sel", 44), "random"),
+    ("eight_ranks_one_expert", Workload("r8", 8, 1, 2, 40, 128, 384, "bf16", "biased",
+                                        "softmax_sel", 45), "random"),
+    ("one_k_block", Workload("k64", 2, 2, 2, 50, 64, 128, "bf16", "uniform",
+                             "softmax_sel", 46), "random"),
+    ("empty_experts", Workload("empty", 4, 4, 2, 30, 256, 512, "bf16", "uniform",
+                               "softmax_sel", 47), "empty"),
+    ("qwen_shape_small", Workload("qwen_small", 8, 16, 8, 48, 1536, 4096, "bf16", "zipf",
+                                  "softmax_sel", 48), "random"),
+]
+
+
+@pytest.mark.parametrize("name,w,kind", EDGE, ids=[e[0] for e in EDGE])
+def test_edge_parity(name, w, kind):
+    routing = make_routing(w)
+    if kind == "hot":
+        ids = np.tile(np.array([2, 3], np.int32), (w.n_ranks, w.tokens, 1))
+        routing = _fixed_routing(w, ids)
+    elif kind == "empty":
+        # only experts 0, 5, 6 and 13 receive rows; every rank keeps at least one empty expert
+        rng = np.random.default_rng(9)
+        choices = np.array([0, 5, 6, 13], np.int32)
+        ids = np.stack([np.stack([rng.choice(choices, 2, replace=False) for _ in range(w.tokens)])
+                        for _ in range(w.n_ranks)])
+        routing = _fixed_routing(w, ids)
+    _check_full(w, routing)
+
+
+def test_identity_weights_bit_exact():
+    """W_e = 2^c I, top_k = 1, gate 1: the whole path moves the activation rows,
+    scaled by a power of two, bit for bit."""
+    w = Workload("ident_gpu", 4, 2, 1, 200, 256, 256, "bf16", "uniform", "softmax_indep", 49)
+    routing, values = make_inputs(w)
+    routing.gates[:] = 1.0
+    for q in range(w.n_ranks):
+        eye = np.stack([np.eye(w.N, dtype=np.float32) * 2.0 ** (e - q)
+                        for e in range(w.n_local_experts)])
+        values[q]["W"] = torch.from_numpy(eye).to(torch.bfloat16).view(torch.int16).numpy().view(
+            np.uint16)
+    s = build_system(w, routing, values)
+    run_all(s, 1)
+    torch.cuda.synchronize()
+    assert (s.status_words() == 0).all()
+    ref = full_pipeline(w, routing, values, epoch=1)
+    for d in range(w.n_ranks):
+        np.testing.assert_array_equal(s.recv[d].cpu().numpy(), ref["recv"][d])
+        np.testing.assert_array_equal(s.out[d].view(torch.int16).cpu().numpy().view(np.uint16),
+                                      ref["out"][d])
+
+
+def test_local_store_when_sink_disabled():
+    """p3_control < 0: rows go to the local C in plan order, nothing is sent or signalled."""
+    w = WORKLOADS["tiny"]
+    routing, values = make_inputs(w)
+    s = build_system(w, routing, values)
+    r = 1
+    m = s.plan_host(r)["m_total"]
+    C = torch.zeros((s.ops[r]["A"].shape[0], w.N), dtype=torch.bfloat16, device="cuda")
+    s.send(r, epoch=7, p3_control=-1, C=C)
+    torch.cuda.synchronize()
+    assert (s.status_words() == 0).all()
+    for d in range(w.n_ranks):  # untouched
+        assert (s.recv[d].cpu().numpy() == 0xFF).all()
+        assert (s.counts[d].cpu().numpy() == -1).all()
+    pl = oracle.plan(w.n_ranks, w.n_local_experts, w.top_k, routing.topk_ids, r)
+    Y = oracle.expert_rows(oracle.BF16, values[r]["A"], values[r]["W"], pl.expert_offsets, w.K,
+                           w.N)
+    got = C[:m].view(torch.int16).cpu().numpy().view(np.uint16)
+    assert max_rel_err(got, Y) <= TOL["bf16"]
