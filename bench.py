@@ -1,0 +1,438 @@
+#!/usr/bin/env python
+"""Benchmark: fused expert-GEMM + combine-scatter step of one logical EP rank.
+
+One step = the whole hot path of one rank on its own batch: the grouped
+down-projection GEMM whose epilogue sends every row to its token's rank
+(grouped_gemm_combine_send, with the completion signalling), then the
+gate-weighted combine of the rank's own tokens (ep_combine_reduce). The other
+logical ranks' receive buffers are separate allocations in the same HBM; their
+producers run once, untimed, before the timed region, and before every step a
+single fill writes their rank flags for the new epoch (the stand-in for peers
+finishing on their own GPUs).
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
+
+Under torchrun each process plays one logical rank (RANK mod n_ranks) on its own
+GPU, independently: replicas with no collective on the data path ("weak"
+scaling); the barrier and max-over-ranks timing use torch.distributed.
+
+The default workload is the Mixtral-like prefill (8 ranks x 1 expert, top-2,
+4096 tokens per rank, 14336 -> 4096 bf16). Every step's inputs (A of that rank:
+~235 MB, its expert weight: ~117 MB) exceed the 129 MB L2, so no explicit flush
+is needed between steps; workloads whose per-step inputs fit in L2 flush it
+with a 512 MB write outside the timed events.
+
+``--impl reference`` times the CPU oracle (the plain C restatement of the path)
+on bounded token samples of the same workload, on the host's cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused expert-GEMM+combine-scatter tokens/s; TFLOP/s and % of roofline"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 10**6
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixtral_prefill")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target host time of the CPU-baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) of SM clocks and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def source_sha(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_traffic(workload: str, kernel: str, src: str):
+    """DRAM bytes per launch of `kernel` from a committed ncu summary, if it was
+    taken on the current source of that kernel."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    rec = d.get(workload, {}).get(kernel)
+    if not rec or rec.get("source_sha") != source_sha(src):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+def algorithmic_work(w, plan_counts: np.ndarray, m_rows: int):
+    """FLOPs and bytes per launch of the two kernels (per logical rank)."""
+    elem = 1 if w.dtype == "fp8_1d2d" else 2
+    nonempty = int((plan_counts.sum(axis=1) > 0).sum())
+    flops = 2.0 * m_rows * w.K * w.N
+    send_bytes = m_rows * w.K * elem + nonempty * w.N * w.K * elem + m_rows * w.N * 2
+    if w.dtype == "fp8_1d2d":
+        send_bytes += m_rows * (w.K // 128) * 4 + nonempty * (w.N // 128) * (w.K // 128) * 4
+    comb_bytes = w.tokens * w.top_k * w.N * 2 + w.tokens * w.N * 2 + w.tokens * w.top_k * 4
+    return flops, float(send_bytes), float(comb_bytes)
+
+
+# ----------------------------------------------------------------- oracle arm
+
+def cpu_sample(w, routing, values, dst: int, target_s: float, plans: dict):
+    """Time the oracle on a token sample of destination `dst`; returns
+    (tokens/s, threads, description)."""
+    import oracle
+    from oracle.pipeline import sampled_pipeline
+
+    rng = np.random.default_rng(123)
+    order = rng.permutation(w.tokens)
+    probe = order[:2]
+    t0 = time.perf_counter()
+    sampled_pipeline(w, routing, lambda r: values[r], dst, probe, plans=plans)
+    per_tok = max((time.perf_counter() - t0) / len(probe), 1e-6)
+    n = int(min(w.tokens, max(4, target_s / per_tok)))
+    toks = np.sort(order[:n])
+    t0 = time.perf_counter()
+    sampled_pipeline(w, routing, lambda r: values[r], dst, toks, plans=plans)
+    dt = time.perf_counter() - t0
+    desc = (f"{n} of rank {dst}'s {w.tokens} tokens: their {w.top_k} expert rows each "
+            f"(GEMM rows from every producer rank) and their combine, {dt:.1f} s")
+    return n / dt, oracle.default_threads(), desc, n, dt
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from synth import WORKLOADS, make_rank_values, make_routing, rows_per_rank
+    import oracle
+
+    w = WORKLOADS[args.workload]
+    routing = make_routing(w)
+    rows = rows_per_rank(w, routing.topk_ids)
+    values = [make_rank_values(w, r, int(rows[r])) for r in range(w.n_ranks)]
+    plans = {r: oracle.plan(w.n_ranks, w.n_local_experts, w.top_k, routing.topk_ids, r)
+             for r in range(w.n_ranks)}
+    budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))  # whole run ~ 2.5 minutes
+    from oracle.pipeline import sampled_pipeline
+    rng = np.random.default_rng(7)
+    t0 = time.perf_counter()
+    sampled_pipeline(w, routing, lambda r: values[r], 0, rng.permutation(w.tokens)[:1],
+                     plans=plans)
+    per_tok = max(time.perf_counter() - t0, 1e-6)
+    n = int(min(w.tokens, max(1, budget / per_tok)))
+    times = []
+    for i in range(args.warmup + args.steps):
+        toks = np.sort(rng.permutation(w.tokens)[:n])
+        t0 = time.perf_counter()
+        sampled_pipeline(w, routing, lambda r: values[r], 0, toks, plans=plans)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    step_s = sum(times) / len(times)
+    value = n / step_s
+    cores = oracle.default_threads()
+    sample = (f"each step: {n} of rank 0's {w.tokens} tokens, their {w.top_k} rows each "
+              f"(GEMM from every producer rank) and their combine")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "n_ranks": w.n_ranks,
+                       "n_local_experts": w.n_local_experts, "top_k": w.top_k,
+                       "tokens_per_rank": w.tokens, "K": w.K, "N": w.N, "my_rank": 0},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------- GPU arm
+
+def main():
+    args = parse_args()
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import moe_expert_gemm_gb300 as ep
+    from moe_expert_gemm_gb300.system import EpSystem
+    from synth import WORKLOADS, make_rank_values, make_routing, rows_per_rank
+
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    ep.load()
+
+    w = WORKLOADS[args.workload]
+    q = rank % w.n_ranks  # the logical rank this process plays
+    routing = make_routing(w)
+    rows = rows_per_rank(w, routing.topk_ids)
+    values = [make_rank_values(w, r, int(rows[r])) for r in range(w.n_ranks)]
+
+    s = EpSystem(w.n_ranks, w.n_local_experts, w.top_k, w.tokens, w.K, w.N, w.dtype)
+    s.set_routing(routing.topk_ids)
+    for r in range(w.n_ranks):
+        s.plan(r)
+        v = values[r]
+        s.set_operands(r, v["A"], v["W"], v.get("a_scales"), v.get("w_scales"))
+    s.set_gates(q, routing.gates[q])
+    # peers' rows land in every receive buffer once (their producers are not timed)
+    for r in range(w.n_ranks):
+        s.send(r, epoch=1)
+    torch.cuda.synchronize()
+    st = s.status_words()
+    if st.any():
+        raise SystemExit(f"device status after staging: {st}")
+    plan_q = s.plan_host(q)
+    m_rows = plan_q["m_total"]
+    flops, send_bytes, comb_bytes = algorithmic_work(w, plan_q["send_counts"], m_rows)
+
+    stream = torch.cuda.current_stream()
+    peer_idx = torch.tensor([w.n_local_experts * w.n_ranks + r for r in range(w.n_ranks)
+                             if r != q], dtype=torch.int64, device="cuda")
+    step_bytes = int(s.ops[q]["A"].numel() * s.ops[q]["A"].element_size()
+                     + s.ops[q]["W"].numel() * s.ops[q]["W"].element_size())
+    flush = torch.empty(512 * 2**20, dtype=torch.uint8, device="cuda") \
+        if step_bytes < 2 * L2_BYTES else None
+    epoch = [2]
+
+    def one_step(evs=None):
+        e = epoch[0]
+        epoch[0] += 1
+        if flush is not None:
+            flush.fill_(e & 0xFF)
+        if peer_idx.numel():
+            s.counts[q].index_fill_(0, peer_idx, e)
+        if evs is not None:
+            evs[0].record(stream)
+        s.send(q, e, stream)
+        if evs is not None:
+            evs[1].record(stream)
+        s.combine(q, e, stream)
+        if evs is not None:
+            evs[2].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        one_step(events[i])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    send_ms = [e[0].elapsed_time(e[1]) for e in events]
+    comb_ms = [e[1].elapsed_time(e[2]) for e in events]
+    step_ms = sum(a + b for a, b in zip(send_ms, comb_ms)) / args.steps
+    st = s.status_words()
+    if st.any():
+        raise SystemExit(f"device status after timing: {st}")
+
+    # ------------------------------------------------------ end to end (host buffers)
+    e2e = None
+    if not args.no_e2e:
+        A_dev = s.ops[q]["A"]
+        A_host = A_dev.cpu().pin_memory()
+        g_host = s.gates[q].cpu().pin_memory()
+        out_host = torch.empty(s.out[q].shape, dtype=s.out[q].dtype).pin_memory()
+        sa_host = s.ops[q]["a_scales"].cpu().pin_memory() if "a_scales" in s.ops[q] else None
+
+        def e2e_step():
+            e = epoch[0]
+            epoch[0] += 1
+            if peer_idx.numel():
+                s.counts[q].index_fill_(0, peer_idx, e)
+            A_dev.copy_(A_host, non_blocking=True)
+            if sa_host is not None:
+                s.ops[q]["a_scales"].copy_(sa_host, non_blocking=True)
+            s.gates[q].copy_(g_host, non_blocking=True)
+            s.send(q, e, stream)
+            s.combine(q, e, stream)
+            out_host.copy_(s.out[q], non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / args.steps
+        h2d = A_host.numel() * A_host.element_size() + g_host.numel() * 4
+        if sa_host is not None:
+            h2d += sa_host.numel() * 4
+        e2e = {"value": w.tokens / (e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())}
+        if world > 1:
+            t = torch.tensor([e2e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e["value"] = world * w.tokens / (float(t.item()) / 1e3)
+        if s.status_words().any():
+            raise SystemExit(f"device status after e2e: {s.status_words()}")
+
+    if world > 1:
+        t = torch.tensor([step_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+
+    peaks, peak_src = load_peaks()
+    send_s = statistics.mean(send_ms) / 1e3
+    comb_s = statistics.mean(comb_ms) / 1e3
+    tflops = flops / send_s / 1e12
+    peak_tf = float(peaks["bf16_tflops"]) * (2.0 if w.dtype == "fp8_1d2d" else 1.0)
+    peak_bw = float(peaks["hbm_gbs"])
+    t_tensor = flops / (peak_tf * 1e12)
+    t_hbm = send_bytes / (peak_bw * 1e9)
+    src = os.path.join(ROOT, "moe_expert_gemm_gb300", "csrc", "ep_gemm_send.cu")
+    traffic = measured_traffic(w.name, "grouped_gemm_combine_send", src)
+    if t_tensor >= t_hbm:
+        roof = {"bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": tflops / peak_tf, "traffic": traffic}
+    else:
+        gbs = send_bytes / send_s / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peak_bw, "unit": "GB/s",
+                "frac": gbs / peak_bw, "traffic": traffic}
+    roof["kernel"] = "grouped_gemm_combine_send"
+    roof["peak_source"] = (f"{peak_src}: " + ("bf16_tflops (burst)" if roof["bound"] == "tensor"
+                                              else "hbm_gbs")
+                           + (" x2 nominal fp8/bf16 ratio" if w.dtype == "fp8_1d2d"
+                              and roof["bound"] == "tensor" else ""))
+    roof["algorithmic_per_launch"] = {"flops": flops, "bytes": send_bytes}
+
+    line = {
+        "metric": METRIC, "value": world * w.tokens / (step_ms / 1e3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "e4m3",
+        "data": "synthetic (seeded; shapes and laws of the named workload)",
+        "config": {"workload": w.name, "n_ranks": w.n_ranks, "n_local_experts": w.n_local_experts,
+                   "top_k": w.top_k, "tokens_per_rank": w.tokens, "K": w.K, "N": w.N,
+                   "operands": w.dtype, "my_rank": q, "rows": m_rows,
+                   "l2": ("flushed with a 512 MB write before every step" if flush is not None
+                          else f"per-step inputs {step_bytes / 1e6:.0f} MB > L2"),
+                   "parallelism": "replicas: one logical rank per GPU" if world > 1
+                   else "one logical rank"},
+        "tflops": tflops,
+        "kernels_ms": {"grouped_gemm_combine_send": statistics.mean(send_ms),
+                       "ep_combine_reduce": statistics.mean(comb_ms)},
+        "combine_gbs": comb_bytes / comb_s / 1e9,
+        "roofline": roof,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        plans = {r: oracle.plan(w.n_ranks, w.n_local_experts, w.top_k, routing.topk_ids, r)
+                 for r in range(w.n_ranks)}
+        v, cores, desc, n, dt = cpu_sample(w, routing, values, q, args.cpu_seconds, plans)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
