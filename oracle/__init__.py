@@ -77,6 +77,11 @@ def lib():
         L.orc_expert_rows.argtypes = ([ctypes.c_int, vp, vp, vp, vp, vp] + [ctypes.c_int] * 3
                                       + [vp, i64, vp, ctypes.c_int])
         L.orc_expert_rows.restype = ctypes.c_int
+        L.orc_expert_rows2.argtypes = ([ctypes.c_int, vp, vp, vp, vp, vp] + [ctypes.c_int] * 3
+                                       + [vp, i64, vp, vp, ctypes.c_int])
+        L.orc_expert_rows2.restype = ctypes.c_int
+        L.orc_combine_exact.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, i64, vp]
+        L.orc_combine_exact.restype = None
         L.orc_scatter.argtypes = ([vp, vp, i64, ctypes.c_int, vp, vp, vp] + [ctypes.c_int] * 3
                                   + [i64, i64, vp, vp])
         L.orc_scatter.restype = i64
@@ -164,8 +169,9 @@ def plan(n_ranks: int, n_local_experts: int, top_k: int, topk_ids: np.ndarray, r
 # ------------------------------------------------------------- expert rows
 
 def expert_rows(dtype: int, A, W, expert_offsets, K: int, N: int, rows=None, a_scales=None,
-                w_scales=None, threads: int | None = None) -> np.ndarray:
-    """bf16 bit patterns [len(rows), N] of the down-projection rows requested."""
+                w_scales=None, threads: int | None = None, exact: bool = False):
+    """bf16 bit patterns [len(rows), N] of the down-projection rows requested;
+    with ``exact`` a pair (bf16 bits, unrounded float64 sums)."""
     El = len(expert_offsets) - 1
     eo = np.ascontiguousarray(expert_offsets, dtype=np.int32)
     if rows is None:
@@ -181,14 +187,15 @@ def expert_rows(dtype: int, A, W, expert_offsets, K: int, N: int, rows=None, a_s
         sa = np.ascontiguousarray(a_scales, dtype=np.float32)
         sw = np.ascontiguousarray(w_scales, dtype=np.float32)
     Y = np.zeros((len(rows), N), np.uint16)
-    if len(rows) == 0:
-        return Y
-    rc = lib().orc_expert_rows(dtype, _p(A), None if sa is None else _p(sa), _p(W),
-                               None if sw is None else _p(sw), _p(eo), El, K, N, _p(rows),
-                               len(rows), _p(Y), threads or default_threads())
-    if rc != 0:
-        raise ValueError(f"orc_expert_rows failed: {rc}")
-    return Y
+    Yd = np.zeros((len(rows), N), np.float64) if exact else None
+    if len(rows):
+        rc = lib().orc_expert_rows2(dtype, _p(A), None if sa is None else _p(sa), _p(W),
+                                    None if sw is None else _p(sw), _p(eo), El, K, N, _p(rows),
+                                    len(rows), _p(Y), None if Yd is None else _p(Yd),
+                                    threads or default_threads())
+        if rc != 0:
+            raise ValueError(f"orc_expert_rows failed: {rc}")
+    return (Y, Yd) if exact else Y
 
 
 # ------------------------------------------------------------------ scatter
@@ -243,6 +250,16 @@ def combine(recv_buf, gates, top_k: int, N: int, msg_bytes: int, tokens=None,
     if len(tokens):
         lib().orc_combine(_p(recv), _p(g), top_k, N, msg_bytes, _p(tokens), len(tokens),
                           _p(out), threads or default_threads())
+    return out
+
+
+def combine_exact(rows_f64, gates) -> np.ndarray:
+    """Exact gate-weighted sums [n, N] of exact rows [n, k, N] (float64, unrounded)."""
+    y = np.ascontiguousarray(rows_f64, dtype=np.float64)
+    g = np.ascontiguousarray(gates, dtype=np.float32)
+    n, k, N = y.shape
+    out = np.zeros((n, N), np.float64)
+    lib().orc_combine_exact(_p(y), _p(g), k, N, n, _p(out))
     return out
 
 

@@ -184,7 +184,8 @@ typedef struct {
     int El, K, N;
     const int64_t *rows;
     int64_t n_rows;
-    uint16_t *Y;
+    uint16_t *Y;   /* bf16 rows, or NULL */
+    double *Yd;    /* unrounded rows, or NULL */
     int64_t lo, hi;
     int status;
 } rows_job;
@@ -238,7 +239,10 @@ static void *rows_worker(void *arg)
             double acc = 0.0;
             for (int kk = 0; kk < j->K; kk++)
                 acc += a[kk] * operand_w(j, e, n, kk);
-            j->Y[r * j->N + n] = orc_bf16_from_double(acc);
+            if (j->Y)
+                j->Y[r * j->N + n] = orc_bf16_from_double(acc);
+            if (j->Yd)
+                j->Yd[r * j->N + n] = acc;
         }
     }
     free(a);
@@ -248,12 +252,13 @@ static void *rows_worker(void *arg)
 /*
  * Down-projection rows of one producer rank: for every requested absolute row m
  * of expert e (expert_offsets[e] <= m < expert_offsets[e+1]),
- * Y[r][n] = bf16(sum_k A[m][k] * W[e][n][k]), r the position of m in `rows`.
+ * Y[r][n] = bf16(sum_k A[m][k] * W[e][n][k]), r the position of m in `rows`;
+ * Yd (if not NULL) receives the same sums unrounded.
  * Returns 0, or -1 if a row lies in no expert.
  */
-int orc_expert_rows(int dtype, const void *A, const float *a_scales, const void *W,
-                    const float *w_scales, const int32_t *expert_offsets, int El, int K, int N,
-                    const int64_t *rows, int64_t n_rows, uint16_t *Y, int nthreads)
+int orc_expert_rows2(int dtype, const void *A, const float *a_scales, const void *W,
+                     const float *w_scales, const int32_t *expert_offsets, int El, int K, int N,
+                     const int64_t *rows, int64_t n_rows, uint16_t *Y, double *Yd, int nthreads)
 {
     if (nthreads < 1)
         nthreads = 1;
@@ -270,7 +275,7 @@ int orc_expert_rows(int dtype, const void *A, const float *a_scales, const void 
         rows_job *j = &jobs[i];
         j->dtype = dtype; j->A = A; j->sa = a_scales; j->W = W; j->sw = w_scales;
         j->expert_offsets = expert_offsets; j->El = El; j->K = K; j->N = N;
-        j->rows = rows; j->n_rows = n_rows; j->Y = Y;
+        j->rows = rows; j->n_rows = n_rows; j->Y = Y; j->Yd = Yd;
         j->lo = n_rows * i / nthreads;
         j->hi = n_rows * (i + 1) / nthreads;
         pthread_create(&th[i], NULL, rows_worker, j);
@@ -284,6 +289,14 @@ int orc_expert_rows(int dtype, const void *A, const float *a_scales, const void 
     free(jobs);
     free(th);
     return status;
+}
+
+int orc_expert_rows(int dtype, const void *A, const float *a_scales, const void *W,
+                    const float *w_scales, const int32_t *expert_offsets, int El, int K, int N,
+                    const int64_t *rows, int64_t n_rows, uint16_t *Y, int nthreads)
+{
+    return orc_expert_rows2(dtype, A, a_scales, W, w_scales, expert_offsets, El, K, N, rows,
+                            n_rows, Y, NULL, nthreads);
 }
 
 /* ----------------------------------------------------------------- scatter */
@@ -392,6 +405,20 @@ static void *combine_worker(void *arg)
         }
     }
     return NULL;
+}
+
+/* The exact gate-weighted sum of exact rows: out[t][n] = sum_j g[t][j] * rows[t][j][n],
+ * no rounding anywhere (the value the rounded path approximates). */
+void orc_combine_exact(const double *rows, const float *gates, int top_k, int N, int64_t n_tokens,
+                       double *out)
+{
+    for (int64_t t = 0; t < n_tokens; t++)
+        for (int n = 0; n < N; n++) {
+            double acc = 0.0;
+            for (int s = 0; s < top_k; s++)
+                acc += (double)gates[t * top_k + s] * rows[(t * top_k + s) * (int64_t)N + n];
+            out[t * N + n] = acc;
+        }
 }
 
 /* Gate-weighted combine of the requested tokens of one destination rank. */

@@ -11,7 +11,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import BF16, FP8_1D2D, Plan, combine, default_threads, expert_rows, plan, scatter, signal
+from . import (BF16, FP8_1D2D, Plan, combine, combine_exact, default_threads, expert_rows, plan,
+               scatter, signal)
 
 SENTINEL_BYTE = 0xFF  # bf16 0xFFFF is a NaN: an unwritten slot cannot pass a value check
 SENTINEL_WORD = np.uint64(0xFFFFFFFFFFFFFFFF)
@@ -27,7 +28,9 @@ def full_pipeline(w, routing, values: list, epoch: int = 1, threads: int | None 
     ``values[r]`` is the operand dict of rank r (``synth.make_rank_values``).
     Returns plans, rows Y per producer, receive buffers / counts per destination,
     election counters per producer, signalling logs per producer, slot hit counts
-    per destination and the combined outputs per destination (bf16 bits)."""
+    per destination, the combined outputs per destination (bf16 bits) and, as
+    ``out_exact`` / ``rows_exact``, the exact combine of the exact rows (float64,
+    no rounding anywhere) per destination."""
     R, El, k, T, K, N = w.n_ranks, w.n_local_experts, w.top_k, w.tokens, w.K, w.N
     msg = w.msg_bytes
     dt = _dtype_code(w.dtype)
@@ -35,13 +38,20 @@ def full_pipeline(w, routing, values: list, epoch: int = 1, threads: int | None 
     counts = [np.full(El * R + R, SENTINEL_WORD, np.uint64) for _ in range(R)]
     hits = np.zeros((R, T * k), np.int32)
     plans, ys, logs, counters = [], [], [], []
+    exact = [np.zeros((T, k, N)) for _ in range(R)]
     bad = 0
     for r in range(R):
         pl = plan(R, El, k, routing.topk_ids, r)
         v = values[r]
-        Y = expert_rows(dt, v["A"], v["W"], pl.expert_offsets, K, N, rows=None,
-                        a_scales=v.get("a_scales"), w_scales=v.get("w_scales"), threads=threads)
+        Y, Yd = expert_rows(dt, v["A"], v["W"], pl.expert_offsets, K, N, rows=None,
+                            a_scales=v.get("a_scales"), w_scales=v.get("w_scales"),
+                            threads=threads, exact=True)
         rows = np.arange(pl.m_total, dtype=np.int64)
+        for m in range(pl.m_total):  # the exact row, placed at its (dst, token, slot)
+            e = int(np.searchsorted(pl.expert_offsets, m, side="right") - 1)
+            dst = int(np.searchsorted(pl.seg_offsets[e], m, side="right") - 1)
+            t, j = pl.src_info[m]
+            exact[dst][t, j] = Yd[m]
         hits, b = scatter(Y, rows, pl, R, k, N, msg, T, recv, hits)
         bad += b
         ctr = np.zeros(R, np.int32)
@@ -50,8 +60,9 @@ def full_pipeline(w, routing, values: list, epoch: int = 1, threads: int | None 
         plans.append(pl)
         ys.append(Y)
     outs = [combine(recv[d], routing.gates[d], k, N, msg, threads=threads) for d in range(R)]
+    out_exact = [combine_exact(exact[d], routing.gates[d]) for d in range(R)]
     return dict(plans=plans, Y=ys, recv=recv, counts=counts, hits=hits, bad=bad, logs=logs,
-                counters=counters, out=outs)
+                counters=counters, out=outs, rows_exact=exact, out_exact=out_exact)
 
 
 def row_of(pl: Plan, src_rank: int, expert_local: int, t: int, j: int) -> int:
@@ -71,7 +82,8 @@ def sampled_pipeline(w, routing, values_of, dst: int, tokens, plans: dict | None
 
     ``values_of(r)`` returns rank r's operand dict. Returns, per sampled token,
     the k received rows (bf16 bits [n, k, N]), the producer (rank, row) of each,
-    and the combined output (bf16 bits [n, N])."""
+    the combined output (bf16 bits [n, N]), and the exact rows and exact combine
+    (float64, unrounded) as ``rows_exact`` / ``out_exact``."""
     R, El, k, N = w.n_ranks, w.n_local_experts, w.top_k, w.N
     dt = _dtype_code(w.dtype)
     tokens = np.asarray(tokens, dtype=np.int64)
@@ -88,19 +100,22 @@ def sampled_pipeline(w, routing, values_of, dst: int, tokens, plans: dict | None
             where[i, j] = (r, m)
             need.setdefault(r, []).append(m)
     rows_out = np.zeros((len(tokens), k, N), np.uint16)
+    rows_exact = np.zeros((len(tokens), k, N), np.float64)
     for r, ms in need.items():
         ms_u = np.unique(np.asarray(ms, dtype=np.int64))
         v = values_of(r)
-        Y = expert_rows(dt, v["A"], v["W"], plans[r].expert_offsets, w.K, N, rows=ms_u,
-                        a_scales=v.get("a_scales"), w_scales=v.get("w_scales"),
-                        threads=threads or default_threads())
+        Y, Yd = expert_rows(dt, v["A"], v["W"], plans[r].expert_offsets, w.K, N, rows=ms_u,
+                            a_scales=v.get("a_scales"), w_scales=v.get("w_scales"),
+                            threads=threads or default_threads(), exact=True)
         pos = {int(m): i for i, m in enumerate(ms_u)}
         for i in range(len(tokens)):
             for j in range(k):
                 if where[i, j, 0] == r:
                     rows_out[i, j] = Y[pos[int(where[i, j, 1])]]
+                    rows_exact[i, j] = Yd[pos[int(where[i, j, 1])]]
     # combine over a compact receive buffer holding just these tokens' slots
     compact = rows_out.reshape(-1).view(np.uint8)
     g = np.ascontiguousarray(routing.gates[dst][tokens])
     out = combine(compact, g, k, N, 2 * N, threads=threads)
-    return dict(tokens=tokens, rows=rows_out, where=where, out=out, plans=plans)
+    return dict(tokens=tokens, rows=rows_out, where=where, out=out, plans=plans,
+                rows_exact=rows_exact, out_exact=combine_exact(rows_exact, g))

@@ -48,7 +48,8 @@ def test_full_size_sampled_parity(name):
     tol = TOL[w.dtype]
     assert max_rel_err(recv0[toks], ref["rows"]) <= tol
     out0 = s.out[0].view(torch.int16).cpu().numpy().view(np.uint16)
-    assert combine_rel_err(out0[toks], ref["out"], ref["rows"], routing.gates[0][toks]) <= tol
+    assert combine_rel_err(out0[toks], ref["out_exact"], ref["rows_exact"],
+                           routing.gates[0][toks]) <= tol
 
     # rows rank 0 produced for the other ranks
     p0 = plans[0]

@@ -36,8 +36,8 @@ def _check_full(w, routing=None, values=None, epoch=3):
         want = ref["recv"][d].view(np.uint16)
         assert max_rel_err(got, want) <= tol, d
         out = s.out[d].view(torch.int16).cpu().numpy().view(np.uint16)
-        rows = want.reshape(w.tokens, w.top_k, w.N)
-        assert combine_rel_err(out, ref["out"][d], rows, routing.gates[d]) <= tol, d
+        assert combine_rel_err(out, ref["out_exact"][d], ref["rows_exact"][d],
+                               routing.gates[d]) <= tol, d
     for r in range(w.n_ranks):  # counters re-armed for the next call
         assert int(s.atomic_counter[r].abs().sum()) == 0
         assert int(s.rank_counter[r].abs().sum()) == 0
@@ -58,8 +58,8 @@ def test_tiny_two_epochs_in_a_row():
     for d in range(w.n_ranks):
         np.testing.assert_array_equal(s.counts[d].cpu().numpy().view(np.uint64), ref2["counts"][d])
         out = s.out[d].view(torch.int16).cpu().numpy().view(np.uint16)
-        rows = ref2["recv"][d].view(np.uint16).reshape(w.tokens, w.top_k, w.N)
-        assert combine_rel_err(out, ref2["out"][d], rows, routing.gates[d]) <= TOL[w.dtype]
+        assert combine_rel_err(out, ref2["out_exact"][d], ref2["rows_exact"][d],
+                               routing.gates[d]) <= TOL[w.dtype]
 
 
 def _fixed_routing(w, ids, seed=5):

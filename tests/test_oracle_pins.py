@@ -226,6 +226,32 @@ def test_expert_rows_bf16_matches_numpy_matmul():
         assert not _ulp_ok(Y[lo:hi], other)
 
 
+def test_unrounded_rows_and_exact_combine_match_numpy():
+    w = WORKLOADS["tiny"]
+    r = make_routing(w)
+    m = rows_per_rank(w, r.topk_ids)
+    vals = [make_rank_values(w, q, int(m[q])) for q in range(w.n_ranks)]
+    pl = oracle.plan(w.n_ranks, w.n_local_experts, w.top_k, r.topk_ids, 2)
+    Y, Yd = oracle.expert_rows(oracle.BF16, vals[2]["A"], vals[2]["W"], pl.expert_offsets, w.K,
+                               w.N, exact=True)
+    A = torch.from_numpy(vals[2]["A"].view(np.int16)).view(torch.bfloat16).double().numpy()
+    W = torch.from_numpy(vals[2]["W"].view(np.int16)).view(torch.bfloat16).double().numpy()
+    for e in range(w.n_local_experts):
+        lo, hi = pl.expert_offsets[e], pl.expert_offsets[e + 1]
+        ref = A[lo:hi] @ W[e].T
+        bound = 1e-12 * (np.abs(A[lo:hi]) @ np.abs(W[e]).T)
+        assert np.all(np.abs(Yd[lo:hi] - ref) <= bound)
+    res = full_pipeline(w, r, vals, epoch=1)
+    for d in range(w.n_ranks):
+        ref = np.einsum("tj,tjn->tn", r.gates[d].astype(np.float64), res["rows_exact"][d])
+        np.testing.assert_allclose(res["out_exact"][d], ref, rtol=1e-12, atol=1e-15)
+        # the rounded path stays within 2^-7 of the terms' scale of the exact value
+        scale = np.einsum("tj,tjn->tn", r.gates[d].astype(np.float64),
+                          np.abs(res["rows_exact"][d]))
+        got = oracle.bf16_to_f64(res["out"][d])
+        assert np.all(np.abs(got - res["out_exact"][d]) <= 2.0**-7 * scale + 1e-30)
+
+
 def test_expert_rows_exact_on_small_integers():
     rng = np.random.default_rng(11)
     El, K, N, M = 3, 16, 24, 10
