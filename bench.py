@@ -53,8 +53,8 @@ L2_BYTES = 129 * 10**6
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixtral_prefill")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -79,7 +79,7 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling (200 ms) of SM clocks and throttle reasons."""
+    """nvidia-smi sampling (100 ms) of SM clocks and throttle reasons."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -97,7 +97,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
                 stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -170,10 +170,16 @@ def cpu_sample(w, routing, values, dst: int, target_s: float, plans: dict):
 
     rng = np.random.default_rng(123)
     order = rng.permutation(w.tokens)
-    probe = order[:2]
-    t0 = time.perf_counter()
-    sampled_pipeline(w, routing, lambda r: values[r], dst, probe, plans=plans)
-    per_tok = max((time.perf_counter() - t0) / len(probe), 1e-6)
+    # calibrate on a growing probe: tiny samples under-use the threads
+    n = min(w.tokens, 16)
+    while True:
+        t0 = time.perf_counter()
+        sampled_pipeline(w, routing, lambda r: values[r], dst, order[:n], plans=plans)
+        dt = time.perf_counter() - t0
+        if dt >= 0.2 * target_s or n >= w.tokens:
+            break
+        n = min(w.tokens, n * 4)
+    per_tok = max(dt / n, 1e-9)
     n = int(min(w.tokens, max(4, target_s / per_tok)))
     toks = np.sort(order[:n])
     t0 = time.perf_counter()
@@ -196,13 +202,14 @@ def run_reference(args, rank, world):
     values = [make_rank_values(w, r, int(rows[r])) for r in range(w.n_ranks)]
     plans = {r: oracle.plan(w.n_ranks, w.n_local_experts, w.top_k, routing.topk_ids, r)
              for r in range(w.n_ranks)}
-    budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))  # whole run ~ 2.5 minutes
+    budget = max(0.1, 150.0 / max(1, args.steps + args.warmup))  # whole run ~ 2.5 minutes
     from oracle.pipeline import sampled_pipeline
     rng = np.random.default_rng(7)
+    probe = min(w.tokens, 16)
     t0 = time.perf_counter()
-    sampled_pipeline(w, routing, lambda r: values[r], 0, rng.permutation(w.tokens)[:1],
+    sampled_pipeline(w, routing, lambda r: values[r], 0, rng.permutation(w.tokens)[:probe],
                      plans=plans)
-    per_tok = max(time.perf_counter() - t0, 1e-6)
+    per_tok = max((time.perf_counter() - t0) / probe, 1e-9)
     n = int(min(w.tokens, max(1, budget / per_tok)))
     times = []
     for i in range(args.warmup + args.steps):
@@ -309,6 +316,7 @@ def main():
         dist.barrier()
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
+    time.sleep(0.5)  # let the sampler start before the timed region
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     torch.cuda.synchronize()
     for i in range(args.steps):
