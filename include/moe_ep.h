@@ -205,6 +205,40 @@ typedef struct {
 int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *args,
                               ep_stream_t stream);
 
+/*
+ * grouped_gemm_combine_send_noalloc -- the same fused GEMM + send for callers
+ * that cannot allocate device memory. The pages have no counterpart to this entry
+ * point; it exists for library users.
+ *
+ * Who needs it: hosts that own every device allocation and forbid allocating
+ * inside their per-call path (an inference engine running kernels from a
+ * plugin's enqueue callback, a serving loop with a fixed memory budget), because
+ * cudaMalloc can implicitly synchronise the device and stall other streams, or
+ * break up a pool the host manages. Such a caller still passes every input and
+ * output in `args`, but not the counter arrays: args->atomic_counter and
+ * args->rank_completion_counter are ignored. The library keeps both in one
+ * file-scope device array of EP_NOALLOC_SCRATCH_INTS int32 words
+ * (EP_MAX_LOCAL_EXPERTS tile counters, then EP_MAX_RANKS election counters;
+ * 1056 bytes) that every GPU loading the library holds until the process exits.
+ *
+ * Behaviour:
+ *  - n_local_experts > EP_MAX_LOCAL_EXPERTS or n_ranks > EP_MAX_RANKS: returns
+ *    EP_ERR_UNSUPPORTED, nothing is enqueued.
+ *  - The first call on a device looks up that device's address of the array
+ *    (with the device current); make that first call before any stream capture.
+ *  - Every call shares the array and it keeps the last call's contents, so each
+ *    call first clears it with an asynchronous memset on `stream` (no allocation).
+ *    Calls that overlap on the GPU (e.g. on two streams at once) race on the
+ *    counters: issue them in order on one stream.
+ *  - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ * Everything else (arguments, results, signalling, status bits) is exactly as for
+ * grouped_gemm_combine_send.
+ */
+#define EP_NOALLOC_SCRATCH_INTS (EP_MAX_LOCAL_EXPERTS + EP_MAX_RANKS)
+
+int grouped_gemm_combine_send_noalloc(const ep_config *cfg, const ep_send_args *args,
+                                      ep_stream_t stream);
+
 /* --------------------------------------------------------------- combine */
 
 /*

@@ -69,7 +69,7 @@ class EpError(RuntimeError):
 _lib = None
 
 EXPORTS = ("ep_plan_sizes", "ep_plan", "grouped_gemm_combine_send", "ep_combine_reduce",
-           "ep_strerror")
+           "ep_strerror", "grouped_gemm_combine_send_noalloc")
 
 
 def load(build_if_missing: bool = True):
@@ -88,7 +88,10 @@ def load(build_if_missing: bool = True):
                                             ctypes.POINTER(ep_send_args), _vp]
     L.ep_combine_reduce.argtypes = [ctypes.POINTER(ep_config), ctypes.POINTER(ep_combine_args),
                                     _vp]
-    for f in ("ep_plan_sizes", "ep_plan", "grouped_gemm_combine_send", "ep_combine_reduce"):
+    L.grouped_gemm_combine_send_noalloc.argtypes = [ctypes.POINTER(ep_config),
+                                                    ctypes.POINTER(ep_send_args), _vp]
+    for f in ("ep_plan_sizes", "ep_plan", "grouped_gemm_combine_send", "ep_combine_reduce",
+              "grouped_gemm_combine_send_noalloc"):
         getattr(L, f).restype = ctypes.c_int
     L.ep_strerror.argtypes = [ctypes.c_int]
     L.ep_strerror.restype = ctypes.c_char_p
@@ -138,6 +141,14 @@ def grouped_gemm_combine_send(cfg: ep_config, args: ep_send_args, stream=None) -
     return _check(load().grouped_gemm_combine_send(ctypes.byref(cfg), ctypes.byref(args),
                                                    stream_handle(stream)),
                   "grouped_gemm_combine_send")
+
+
+def grouped_gemm_combine_send_noalloc(cfg: ep_config, args: ep_send_args, stream=None) -> int:
+    """The fused send for callers that cannot allocate: the counter arrays come
+    from the library's own device array (args' counter pointers are ignored)."""
+    return _check(load().grouped_gemm_combine_send_noalloc(ctypes.byref(cfg), ctypes.byref(args),
+                                                           stream_handle(stream)),
+                  "grouped_gemm_combine_send_noalloc")
 
 
 def ep_combine_reduce(cfg: ep_config, args: ep_combine_args, stream=None) -> int:
