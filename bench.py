@@ -61,6 +61,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target host time of the CPU-baseline sample")
+    ap.add_argument("--trace", default=None,
+                    help="after timing, run one traced send and write its summary here")
     return ap.parse_args()
 
 
@@ -331,6 +333,17 @@ def main():
     st = s.status_words()
     if st.any():
         raise SystemExit(f"device status after timing: {st}")
+
+    if args.trace and rank == 0:
+        from moe_expert_gemm_gb300.system import summarize_trace
+        e = epoch[0]
+        epoch[0] += 1
+        s.counts[q].index_fill_(0, peer_idx, e)
+        tr = s.send_traced(q, e, records=256)
+        s.combine(q, e, stream)
+        torch.cuda.synchronize()
+        with open(args.trace, "w") as f:
+            json.dump({"workload": w.name, "summary": summarize_trace(tr), "blocks": tr}, f)
 
     # ------------------------------------------------------ end to end (host buffers)
     e2e = None

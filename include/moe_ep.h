@@ -165,8 +165,17 @@ int ep_plan(const ep_config *cfg, const int32_t *topk_ids, const ep_plan_out *ou
  *                    ("EpiloguePeerSink" p3_control: negative disables the sink).
  *   C                [max_rows][N] bf16, used only when p3_control < 0.
  *   status           device word for EP_STATUS_* bits.
- *   trace            reserved: must be NULL.
+ *   trace            optional (NULL: off) per-tile timestamps ("P3PeerSendConfig" fields
+ *                    trace_ptr / trace_on / send_stamp_ptr): thread block b owns the
+ *                    2 + 4*trace_records words starting at b*(2 + 4*trace_records):
+ *                    [0] tiles it processed, [1] %globaltimer (ns) at its start, then
+ *                    one record per tile (the first trace_records tiles):
+ *                    {tile | expert << 32 | completed-the-expert << 63,
+ *                     time the accumulator was ready, time the tile's rows were all
+ *                     stored, time its completion counting (and signalling) ended}.
+ *                    Allocate at least (#SMs) * (2 + 4*trace_records) words.
  *   timeout_ns       limit of each bounded wait inside the kernel (0: 2 s).
+ *   trace_records    records per thread block in `trace` (>= 1 when trace is set).
  */
 typedef struct {
     const void *A;
@@ -188,6 +197,7 @@ typedef struct {
     uint32_t *status;
     uint64_t *trace;
     int64_t timeout_ns;
+    int64_t trace_records;
 } ep_send_args;
 
 /*

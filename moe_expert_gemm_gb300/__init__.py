@@ -52,7 +52,7 @@ class ep_send_args(ctypes.Structure):
                 ("recv_buf_ptrs", _vp * EP_MAX_RANKS), ("recv_count_ptrs", _vp * EP_MAX_RANKS),
                 ("atomic_counter", _vp), ("rank_completion_counter", _vp), ("epoch", _c_u64),
                 ("p3_control", _c_i32), ("C", _vp), ("status", _vp), ("trace", _vp),
-                ("timeout_ns", _c_i64)]
+                ("timeout_ns", _c_i64), ("trace_records", _c_i64)]
 
 
 class ep_combine_args(ctypes.Structure):

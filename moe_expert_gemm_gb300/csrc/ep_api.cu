@@ -161,7 +161,10 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     const int R = cfg->n_ranks;
     const bool sink = a->p3_control >= 0;
     if (!a->A || !a->W || !a->expert_offsets || !a->src_info || !a->seg_offsets ||
-        !a->send_counts || !a->status || a->trace)
+        !a->send_counts || !a->status)
+        return EP_ERR_INVALID_ARG;
+    if (a->trace && (a->trace_records < 1 || a->trace_records > (1 << 20) ||
+                     (reinterpret_cast<uintptr_t>(a->trace) & 7u)))
         return EP_ERR_INVALID_ARG;
     if (!aligned16(a->A) || !aligned16(a->W))
         return EP_ERR_INVALID_ARG;
@@ -222,6 +225,8 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     p.timeout_ns = a->timeout_ns > 0 ? static_cast<uint64_t>(a->timeout_ns) : kDefaultTimeoutNs;
     p.a_scales = a->a_scales;
     p.w_scales = a->w_scales;
+    p.trace = a->trace;
+    p.trace_records = a->trace ? static_cast<int>(a->trace_records) : 0;
 
     // the plan lives on the device, so size the grid by the worst-case tile count
     const int64_t max_tiles = ((a->max_rows + ep::BM - 1) / ep::BM + El) * p.n_blocks;

@@ -279,6 +279,11 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t stg = smem_u32(smem + L::kOffStaging + (warp - 2) * L::kWarpStaging);
         const int R = p.n_ranks;
 
+        uint64_t *trace = nullptr;  // this block's trace words (thread epi_tid 0 only)
+        if (p.trace && epi_tid == 0) {
+            trace = p.trace + static_cast<int64_t>(blockIdx.x) * (2 + 4 * p.trace_records);
+            trace[1] = globaltimer_ns();
+        }
         if (p.sink_enabled && blockIdx.x == 0 && epi_tid == 0) {
             // experts without rows have no tile to complete: signal their zero counts now
             for (int e = 0; e < El; ++e)
@@ -321,6 +326,11 @@ __global__ void __launch_bounds__(192, 1)
             if (!ok)
                 break;
             tc_fence_after();
+            uint64_t *rec = (trace && i < p.trace_records) ? trace + 2 + 4 * i : nullptr;
+            if (rec) {
+                rec[0] = static_cast<uint64_t>(t) | (static_cast<uint64_t>(c.e) << 32);
+                rec[1] = globaltimer_ns();
+            }
 
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(as * BN);
@@ -369,16 +379,26 @@ __global__ void __launch_bounds__(192, 1)
                 // all 128 sink threads' stores of this tile precede the count increment
                 named_bar_sync(1, 128);
                 if (epi_tid == 0) {
+                    if (rec)
+                        rec[2] = globaltimer_ns();
                     const int tiles_e =
                         (c.m_end - s_eoff[c.e] + BM - 1) / BM * p.n_blocks;
                     const int old = atom_add_acq_rel_gpu(&p.atomic_counter[c.e], 1);
                     if (old == tiles_e - 1) {
                         *reinterpret_cast<volatile int *>(&p.atomic_counter[c.e]) = 0;
                         signal_expert(p, c.e, s_cnt);
+                        if (rec)
+                            rec[0] |= 1ull << 63;
                     }
+                    if (rec)
+                        rec[3] = globaltimer_ns();
                 }
+            } else if (rec) {
+                rec[2] = rec[3] = globaltimer_ns();
             }
         }
+        if (trace)
+            trace[0] = static_cast<uint64_t>(i);
         if (!ok && lane == 0)
             raise_abort(p.status, abort_flag);
     }

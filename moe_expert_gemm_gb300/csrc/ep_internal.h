@@ -35,6 +35,8 @@ struct SendParams {
     uint64_t timeout_ns;
     const float *a_scales;
     const float *w_scales;
+    uint64_t *trace;    // optional per-tile timestamps
+    int trace_records;  // records per thread block
 };
 
 struct PlanParams {

@@ -138,6 +138,18 @@ class EpSystem:
         grouped_gemm_combine_send(self.cfg(rank), self.send_args(rank, epoch, p3_control, C),
                                   stream)
 
+    def send_traced(self, rank: int, epoch: int, records: int = 64, stream=None):
+        """One send with per-tile timestamps; returns the decoded trace."""
+        n_sm = torch.cuda.get_device_properties(self.device).multi_processor_count
+        stride = 2 + 4 * records
+        buf = torch.zeros(n_sm * stride, dtype=torch.int64, device=self.device)
+        a = self.send_args(rank, epoch)
+        a.trace = ptr(buf)
+        a.trace_records = records
+        grouped_gemm_combine_send(self.cfg(rank), a, stream)
+        torch.cuda.synchronize()
+        return decode_trace(buf.cpu().numpy().view(np.uint64), n_sm, records)
+
     def combine_args(self, rank: int, epoch: int, gates=None, out=None) -> ep_combine_args:
         g = self.gates[rank] if gates is None else gates
         o = self.out[rank] if out is None else out
@@ -168,3 +180,48 @@ class EpSystem:
                     seg_offsets=p["seg_offsets"].cpu().numpy(),
                     send_counts=p["send_counts"].cpu().numpy(),
                     gather_idx=p["gather_idx"][:m].cpu().numpy(), m_total=m)
+
+
+def decode_trace(words: np.ndarray, n_blocks: int, records: int) -> list:
+    """Per thread block: start time and one record per traced tile
+    (tile, expert, completed_expert, t_ready, t_stored, t_done), times in ns."""
+    stride = 2 + 4 * records
+    out = []
+    for b in range(n_blocks):
+        w = words[b * stride:(b + 1) * stride]
+        n = int(w[0])
+        recs = []
+        for i in range(min(n, records)):
+            r = w[2 + 4 * i:6 + 4 * i]
+            recs.append(dict(tile=int(r[0] & 0xFFFFFFFF), expert=int((r[0] >> 32) & 0x7FFFFFFF),
+                             completed=bool(r[0] >> 63), t_ready=int(r[1]), t_stored=int(r[2]),
+                             t_done=int(r[3])))
+        out.append(dict(tiles=n, t_start=int(w[1]), records=recs))
+    return out
+
+
+def summarize_trace(tr: list) -> dict:
+    """Where a fused launch spends its time, from a decoded trace."""
+    starts = [b["t_start"] for b in tr if b["t_start"]]
+    recs = [r for b in tr for r in b["records"]]
+    if not starts or not recs:
+        return {}
+    t0 = min(starts)
+    t1 = max(r["t_done"] for r in recs)
+    epi = [r["t_stored"] - r["t_ready"] for r in recs]
+    cnt = [r["t_done"] - r["t_stored"] for r in recs if not r["completed"]]
+    sig = [r["t_done"] - r["t_stored"] for r in recs if r["completed"]]
+    waits = []
+    for b in tr:
+        prev = b["t_start"]
+        for r in b["records"]:
+            waits.append(r["t_ready"] - prev)
+            prev = r["t_done"]
+    last_end = [max(r["t_done"] for r in b["records"]) - t0 for b in tr if b["records"]]
+
+    def st(x):
+        x = np.asarray(x, dtype=np.float64) / 1e3
+        return {} if x.size == 0 else dict(n=int(x.size), mean_us=float(x.mean()),
+                                           p50_us=float(np.median(x)), max_us=float(x.max()))
+    return dict(span_us=(t1 - t0) / 1e3, tiles=len(recs), epilogue=st(epi), count=st(cnt),
+                signal=st(sig), wait_for_accumulator=st(waits), block_end=st(last_end))

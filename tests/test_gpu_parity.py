@@ -148,3 +148,25 @@ def test_local_store_when_sink_disabled():
                            w.N)
     got = C[:m].view(torch.int16).cpu().numpy().view(np.uint16)
     assert max_rel_err(got, Y) <= TOL["bf16"]
+
+
+def test_trace_records_every_tile_once():
+    """Optional per-tile timestamps: every tile appears once, times are ordered,
+    and exactly the non-empty experts are marked as completed once each."""
+    w = Workload("trace_small", 4, 4, 2, 300, 256, 512, "bf16", "zipf", "softmax_sel", 50)
+    routing, values = make_inputs(w)
+    s = build_system(w, routing, values)
+    for r in range(w.n_ranks):
+        s.send(r, epoch=1)
+    tr = s.send_traced(1, epoch=2, records=64)
+    assert (s.status_words() == 0).all()
+    recs = [rec for b in tr for rec in b["records"]]
+    assert sum(b["tiles"] for b in tr) == len(recs)
+    pl = oracle.plan(w.n_ranks, w.n_local_experts, w.top_k, routing.topk_ids, 1)
+    rows = np.diff(pl.expert_offsets)
+    n_blocks = w.N // 256
+    assert sorted(r["tile"] for r in recs) == list(range(int((-(-rows // 128)).sum()) * n_blocks))
+    assert all(b["t_start"] <= r["t_ready"] <= r["t_stored"] <= r["t_done"]
+               for b in tr for r in b["records"])
+    done = sorted(r["expert"] for r in recs if r["completed"])
+    assert done == [e for e in range(w.n_local_experts) if rows[e] > 0]
