@@ -8,7 +8,7 @@
 // (src_idx*top_k + src_topk)*msg_bytes + byte_off.
 //
 // HBM-bound: every received byte is read once and every output byte written
-// once. One thread per block acquires all source flags (bounded wait), then each
+// once. R threads per block acquire the R source flags (bounded waits), then each
 // warp handles 256 contiguous columns of one token: 32 lanes x 16-byte loads of
 // each of the token's top_k rows, fp32 accumulation in slot order, one 16-byte
 // streaming store. The grid is one wave of 8 blocks per SM with a grid-stride loop.
@@ -34,22 +34,21 @@ __device__ __forceinline__ void accumulate_row(float (&acc)[8], float g, uint4 r
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p)
 {
     __shared__ int s_ok;
-    if (threadIdx.x == 0) {
-        bool ok = true;
-        const uint64_t *flags = p.recv_count + static_cast<int64_t>(p.El) * p.n_ranks;
+    if (threadIdx.x == 0)
+        s_ok = 1;
+    __syncthreads();
+    if (threadIdx.x < p.n_ranks) {
+        // one thread per source rank acquires that rank's flag (bounded wait)
+        const uint64_t *flag = p.recv_count + static_cast<int64_t>(p.El) * p.n_ranks + threadIdx.x;
         const uint64_t t0 = globaltimer_ns();
-        for (int rk = 0; rk < p.n_ranks && ok; ++rk) {
-            while (ld_acquire_sys_u64(flags + rk) != p.epoch) {
-                if (globaltimer_ns() - t0 > p.timeout_ns) {
-                    ok = false;
-                    break;
-                }
-                __nanosleep(100);
+        while (ld_acquire_sys_u64(flag) != p.epoch) {
+            if (globaltimer_ns() - t0 > p.timeout_ns) {
+                atomicOr(p.status, EP_STATUS_TIMEOUT);
+                s_ok = 0;
+                break;
             }
+            __nanosleep(100);
         }
-        if (!ok)
-            atomicOr(p.status, EP_STATUS_TIMEOUT);
-        s_ok = ok;
     }
     __syncthreads();
     if (!s_ok)

@@ -49,10 +49,13 @@ struct GemmLayout {
     static constexpr int kOffPtrs = (kOffAbort + 4 + 15) / 16 * 16;  // 8 recv_buf + 8 recv_count
     static constexpr int kOffTileStart = kOffPtrs + 16 * 8;
     static constexpr int kOffExpertOff = kOffTileStart + 4 * (EP_MAX_LOCAL_EXPERTS + 1);
-    static constexpr int kEnd = kOffExpertOff + 4 * (EP_MAX_LOCAL_EXPERTS + 1);
+    static constexpr int kQueue = 64;  // tile-completion queue, epilogue -> completion warp
+    static constexpr int kOffQueue = (kOffExpertOff + 4 * (EP_MAX_LOCAL_EXPERTS + 1) + 15) / 16 * 16;
+    static constexpr int kOffQueueCtl = kOffQueue + 16 * kQueue;  // head, tail, done
+    static constexpr int kEnd = kOffQueueCtl + 16;
     static constexpr int kSmemBytes = kEnd + 1024;  // slack to align the base to 1024
     static constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators
-    static constexpr int kThreads = 192;
+    static constexpr int kThreads = 224;            // TMA, MMA, 4 epilogue, completion
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM columns");
 };
@@ -63,22 +66,41 @@ __device__ __forceinline__ void raise_abort(uint32_t *status, volatile int *abor
     *abort_flag = 1;
 }
 
-// Completion signalling of local expert e towards every destination rank.
+// Completion signalling of local expert e towards every destination rank
+// ("ep_signal_completion", ep_ord_r with has_rank_flag). The caller has acquired
+// every row of expert e. For each destination: a plain progress store of the count
+// word, then the election on that destination's counter. The release half of the
+// acquire-release election is one system-scope fence ahead of all R increments
+// (it releases the rows and the count words); the acquire half is a second fence,
+// taken only when this call is elected for some destination, which also orders
+// the rank-flag stores after everything the other experts released.
 __device__ void signal_expert(const SendParams &p, int e, uint64_t *const *cnt)
 {
     const int R = p.n_ranks;
     for (int dst = 0; dst < R; ++dst) {
-        uint64_t *words = cnt[dst];
-        // plain progress store of the count word, recv_count_layout((e, my_rank))
-        volatile uint64_t *w = words + static_cast<int64_t>(e) * R + p.my_rank;
+        volatile uint64_t *w = cnt[dst] + static_cast<int64_t>(e) * R + p.my_rank;
         *w = static_cast<uint64_t>(p.send_counts[e * R + dst]);
-        // election: releases this producer's payload and count, acquires its predecessors'
-        const int old = atom_add_acq_rel_sys(&p.rank_counter[dst], 1);
-        if (old == p.El - 1) {
+    }
+    fence_acq_rel_sys();
+    int old[EP_MAX_RANKS];
+#pragma unroll
+    for (int dst = 0; dst < EP_MAX_RANKS; ++dst)
+        if (dst < R)
+            old[dst] = atom_add_relaxed_sys(&p.rank_counter[dst], 1);
+    bool elected = false;
+#pragma unroll
+    for (int dst = 0; dst < EP_MAX_RANKS; ++dst)
+        elected |= dst < R && old[dst] == p.El - 1;
+    if (!elected)
+        return;
+    fence_acq_rel_sys();
+#pragma unroll
+    for (int dst = 0; dst < EP_MAX_RANKS; ++dst) {
+        if (dst < R && old[dst] == p.El - 1) {
             // last expert of this rank for dst: re-arm the counter for the next call and
-            // publish the whole rank with one system-scope release of the rank flag
+            // publish the whole rank through the rank flag
             *reinterpret_cast<volatile int *>(&p.rank_counter[dst]) = 0;
-            st_release_sys_u64(words + static_cast<int64_t>(p.El) * R + p.my_rank, p.epoch);
+            st_relaxed_sys_u64(cnt[dst] + static_cast<int64_t>(p.El) * R + p.my_rank, p.epoch);
         }
     }
 }
@@ -110,7 +132,7 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const int *tile_start, c
 }
 
 template <int BN, int STAGES>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     gemm_send_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a,
                           const __grid_constant__ CUtensorMap tmap_b,
                           const __grid_constant__ SendParams p)
@@ -133,6 +155,10 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t **s_cnt = reinterpret_cast<uint64_t **>(smem + L::kOffPtrs + 64);
     int *s_tile_start = reinterpret_cast<int *>(smem + L::kOffTileStart);
     int *s_eoff = reinterpret_cast<int *>(smem + L::kOffExpertOff);
+    int4 *s_queue = reinterpret_cast<int4 *>(smem + L::kOffQueue);
+    volatile int *q_head = reinterpret_cast<volatile int *>(smem + L::kOffQueueCtl);
+    volatile int *q_tail = q_head + 1;
+    volatile int *q_done = q_head + 2;
     const int El = p.El;
 
     // ---------------------------------------------------------------- prologue
@@ -147,18 +173,25 @@ __global__ void __launch_bounds__(192, 1)
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
+        *q_head = 0;
+        *q_tail = 0;
+        *q_done = 0;
         fence_mbar_init();
     }
     if (threadIdx.x < EP_MAX_RANKS) {
         s_recv[threadIdx.x] = p.recv_buf[threadIdx.x];
         s_cnt[threadIdx.x] = p.recv_count[threadIdx.x];
     }
+    // expert row ranges: one load per thread, then one thread makes them monotone and
+    // clamped to the rows of A (so a malformed plan cannot send reads past the plan
+    // arrays) and builds the tile table
+    for (int e = threadIdx.x; e <= El; e += blockDim.x)
+        s_eoff[e] = __ldg(p.expert_offsets + e);
+    __syncthreads();
     if (threadIdx.x == 32) {
-        // expert row ranges, made monotone and clamped to the rows of A so that a
-        // malformed plan cannot send reads past the plan arrays
         int prev = 0;
         for (int e = 0; e <= El; ++e) {
-            int v = p.expert_offsets[e];
+            int v = s_eoff[e];
             v = v < prev ? prev : v;
             v = v > p.max_rows ? static_cast<int>(p.max_rows) : v;
             s_eoff[e] = v;
@@ -272,7 +305,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_wait(mma_done, 0, p.timeout_ns, &no_abort);
         }
         __syncwarp();
-    } else {
+    } else if (warp < 6) {
         // --------------------------------------------------- epilogue + sink
         const int q = warp & 3;  // TMEM lane quarter this warp may read
         const int epi_tid = threadIdx.x - 64;
@@ -284,14 +317,8 @@ __global__ void __launch_bounds__(192, 1)
             trace = p.trace + static_cast<int64_t>(blockIdx.x) * (2 + 4 * p.trace_records);
             trace[1] = globaltimer_ns();
         }
-        if (p.sink_enabled && blockIdx.x == 0 && epi_tid == 0) {
-            // experts without rows have no tile to complete: signal their zero counts now
-            for (int e = 0; e < El; ++e)
-                if (s_eoff[e + 1] == s_eoff[e])
-                    signal_expert(p, e, s_cnt);
-        }
-
         bool ok = true;
+        bool push_ok = true;  // epi_tid 0: the last hand-off to the completion warp succeeded
         int i = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++i) {
             const TileCoord c = decode_tile(t, s_tile_start, s_eoff, El, p.n_blocks);
@@ -321,8 +348,10 @@ __global__ void __launch_bounds__(192, 1)
                 }
             }
 
-            ok = mbar_wait(&acc_full[as], aphase, p.timeout_ns, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
+            ok = mbar_wait(&acc_full[as], aphase, p.timeout_ns, abort_flag) && push_ok;
+            // all four epilogue warps take the same decision, so none is left waiting
+            // at a named barrier that another has abandoned
+            ok = named_bar_and(2, 128, ok);
             if (!ok)
                 break;
             tc_fence_after();
@@ -376,31 +405,110 @@ __global__ void __launch_bounds__(192, 1)
                 mbar_arrive(&acc_empty[as]);
 
             if (p.sink_enabled) {
-                // all 128 sink threads' stores of this tile precede the count increment
+                // all 128 sink threads' stores of this tile precede the hand-off to the
+                // completion warp, which counts the tile
                 named_bar_sync(1, 128);
                 if (epi_tid == 0) {
                     if (rec)
                         rec[2] = globaltimer_ns();
-                    const int tiles_e =
-                        (c.m_end - s_eoff[c.e] + BM - 1) / BM * p.n_blocks;
-                    const int old = atom_add_acq_rel_gpu(&p.atomic_counter[c.e], 1);
-                    if (old == tiles_e - 1) {
-                        *reinterpret_cast<volatile int *>(&p.atomic_counter[c.e]) = 0;
-                        signal_expert(p, c.e, s_cnt);
-                        if (rec)
-                            rec[0] |= 1ull << 63;
+                    const int tiles_e = (c.m_end - s_eoff[c.e] + BM - 1) / BM * p.n_blocks;
+                    // bounded wait for a free queue slot; a failure is voted on at the
+                    // next tile (or reported after the loop)
+                    const uint64_t t0 = globaltimer_ns();
+                    while (*q_tail - *q_head >= L::kQueue) {
+                        if (*abort_flag || globaltimer_ns() - t0 > p.timeout_ns) {
+                            push_ok = false;
+                            break;
+                        }
                     }
-                    if (rec)
-                        rec[3] = globaltimer_ns();
+                    if (push_ok) {
+                        const int tl = *q_tail;
+                        s_queue[tl % L::kQueue] = make_int4(c.e, rec ? i : -1, tiles_e, 0);
+                        __threadfence_block();
+                        *q_tail = tl + 1;
+                    }
                 }
             } else if (rec) {
                 rec[2] = rec[3] = globaltimer_ns();
             }
         }
-        if (trace)
-            trace[0] = static_cast<uint64_t>(i);
+        if (epi_tid == 0) {
+            if (trace)
+                trace[0] = static_cast<uint64_t>(i);
+            __threadfence_block();
+            *q_done = 1;
+            if (!push_ok)
+                raise_abort(p.status, abort_flag);
+        }
         if (!ok && lane == 0)
             raise_abort(p.status, abort_flag);
+    } else if (warp == 6) {
+        // ------------------------------------------- completion counting + signalling
+        // Runs beside the epilogue so that neither the per-tile release fence nor the
+        // system-scope signalling ever stalls the output path.
+        if (lane == 0 && p.sink_enabled) {
+            uint64_t *trace =
+                p.trace ? p.trace + static_cast<int64_t>(blockIdx.x) * (2 + 4 * p.trace_records)
+                        : nullptr;
+            if (blockIdx.x == 0) {
+                // experts without rows have no tile to complete: signal their zero counts
+                for (int e = 0; e < El; ++e)
+                    if (s_eoff[e + 1] == s_eoff[e])
+                        signal_expert(p, e, s_cnt);
+            }
+            int head = 0;
+            uint64_t t0 = globaltimer_ns();
+            while (true) {
+                const int tail = *q_tail;
+                if (head < tail) {
+                    __threadfence_block();
+                    int4 ent[8];
+                    int n = 0;
+                    while (head < tail && n < 8)
+                        ent[n++] = s_queue[(head++) % L::kQueue];
+                    __threadfence_block();
+                    *q_head = head;
+                    // one release fence covers the rows of every tile popped here
+                    fence_acq_rel_gpu();
+                    bool last[8];
+                    bool any = false;
+                    for (int j = 0; j < n; ++j) {
+                        const int old = atom_add_relaxed_gpu(&p.atomic_counter[ent[j].x], 1);
+                        last[j] = old == ent[j].z - 1;
+                        any |= last[j];
+                    }
+                    if (any)
+                        fence_acq_rel_gpu();  // acquire the expert's other tiles
+                    for (int j = 0; j < n; ++j) {
+                        if (last[j]) {
+                            *reinterpret_cast<volatile int *>(&p.atomic_counter[ent[j].x]) = 0;
+                            signal_expert(p, ent[j].x, s_cnt);
+                        }
+                        if (trace && ent[j].y >= 0) {
+                            uint64_t *rec = trace + 2 + 4 * ent[j].y;
+                            if (last[j])
+                                rec[0] |= 1ull << 63;
+                            rec[3] = globaltimer_ns();
+                        }
+                    }
+                    t0 = globaltimer_ns();
+                    continue;
+                }
+                if (*q_done) {
+                    __threadfence_block();
+                    if (*q_tail == head)
+                        break;
+                    continue;
+                }
+                if (*abort_flag)
+                    break;
+                if (globaltimer_ns() - t0 > p.timeout_ns) {
+                    raise_abort(p.status, abort_flag);
+                    break;
+                }
+            }
+        }
+        __syncwarp();
     }
 
     // --------------------------------------------------------------- teardown

@@ -250,6 +250,27 @@ __device__ __forceinline__ int atom_add_acq_rel_sys(int *p, int v)
     return old;
 }
 
+__device__ __forceinline__ int atom_add_relaxed_gpu(int *p, int v)
+{
+    int old;
+    asm volatile("atom.relaxed.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
+__device__ __forceinline__ int atom_add_relaxed_sys(int *p, int v)
+{
+    int old;
+    asm volatile("atom.relaxed.sys.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void fence_acq_rel_sys()
+{
+    asm volatile("fence.acq_rel.sys;" ::: "memory");
+}
+
 __device__ __forceinline__ void st_release_sys_u64(uint64_t *p, uint64_t v)
 {
     asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
@@ -275,6 +296,22 @@ __device__ __forceinline__ void fence_acq_rel_gpu()
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier over `nthreads` threads that also ANDs a predicate across them:
+// every participant returns the same decision.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pin, pout;\n\t"
+        "setp.ne.u32 pin, %1, 0;\n\t"
+        "bar.red.and.pred pout, %2, %3, pin;\n\t"
+        "selp.u32 %0, 1, 0, pout;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 // 16-byte global store / shared load.
