@@ -154,10 +154,19 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
         return rc;
     if (!a)
         return EP_ERR_INVALID_ARG;
-    if (cfg->dtype != EP_BF16 || cfg->send_warps == 4)
+    const bool fp8 = cfg->dtype == EP_FP8_1D2D;
+    if (cfg->send_warps == 4)
         return EP_ERR_UNSUPPORTED;
-    if (cfg->K % 64 != 0 || cfg->N % 64 != 0)
+    if (!fp8 && (cfg->K % 64 != 0 || cfg->N % 64 != 0))
         return EP_ERR_UNSUPPORTED;  // whole 128-byte K atoms and 64-column output chunks
+    // fp8: one 128-wide scale block per K step and 256-column tiles (two weight-scale
+    // blocks each)
+    if (fp8 && (cfg->K % 128 != 0 || cfg->N % 256 != 0))
+        return EP_ERR_UNSUPPORTED;
+    if (fp8 && (!a->a_scales || !a->w_scales ||
+                (reinterpret_cast<uintptr_t>(a->a_scales) & 3u) ||
+                (reinterpret_cast<uintptr_t>(a->w_scales) & 3u)))
+        return EP_ERR_INVALID_ARG;
     const int R = cfg->n_ranks;
     const bool sink = a->p3_control >= 0;
     if (!a->A || !a->W || !a->expert_offsets || !a->src_info || !a->seg_offsets ||
@@ -184,15 +193,18 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     if (num_sms <= 0)
         return EP_ERR_CUDA;
 
-    const int bn = cfg->N % 256 == 0 ? 256 : (cfg->N % 128 == 0 ? 128 : 64);
+    const int bn = fp8 ? 256 : (cfg->N % 256 == 0 ? 256 : (cfg->N % 128 == 0 ? 128 : 64));
     const int El = cfg->n_local_experts;
+    const int elem = fp8 ? 1 : 2;
+    const int box_k = 128 / elem;  // one 128-byte swizzle atom of K per stage
+    const CUtensorMapDataType dt =
+        fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap ta, tb;
-    if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->A, cfg->K, a->max_rows,
-                   static_cast<uint64_t>(cfg->K) * 2, 64, ep::BM))
+    if (!encode_2d(&ta, dt, a->A, cfg->K, a->max_rows, static_cast<uint64_t>(cfg->K) * elem,
+                   box_k, ep::BM))
         return EP_ERR_CUDA;
-    if (!encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->W, cfg->K,
-                   static_cast<uint64_t>(El) * cfg->N, static_cast<uint64_t>(cfg->K) * 2, 64,
-                   static_cast<uint32_t>(bn)))
+    if (!encode_2d(&tb, dt, a->W, cfg->K, static_cast<uint64_t>(El) * cfg->N,
+                   static_cast<uint64_t>(cfg->K) * elem, box_k, static_cast<uint32_t>(bn)))
         return EP_ERR_CUDA;
 
     ep::SendParams p;
@@ -205,7 +217,7 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     p.N = cfg->N;
     p.max_tokens = cfg->max_tokens_per_rank;
     p.n_blocks = cfg->N / bn;
-    p.num_k_blocks = cfg->K / 64;
+    p.num_k_blocks = cfg->K / box_k;
     p.msg_bytes = cfg->msg_bytes;
     p.max_rows = a->max_rows;
     p.expert_offsets = a->expert_offsets;
@@ -232,8 +244,9 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     const int64_t max_tiles = ((a->max_rows + ep::BM - 1) / ep::BM + El) * p.n_blocks;
     const int grid = static_cast<int>(max_tiles < num_sms ? (max_tiles < 1 ? 1 : max_tiles)
                                                           : num_sms);
-    return cuda_status(
-        ep::launch_gemm_send_bf16(ta, tb, p, bn, grid, reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return cuda_status(fp8 ? ep::launch_gemm_send_fp8(ta, tb, p, grid, s)
+                           : ep::launch_gemm_send_bf16(ta, tb, p, bn, grid, s));
 }
 
 int ep_combine_reduce(const ep_config *cfg, const ep_combine_args *a, ep_stream_t stream)

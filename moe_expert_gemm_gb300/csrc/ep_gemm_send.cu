@@ -1,4 +1,4 @@
-// Grouped expert GEMM with the EP-combine send fused into its epilogue.
+// Grouped expert GEMM (bf16) with the EP-combine send fused into its epilogue.
 //
 // "EpiloguePeerSink" (Modular MAX Mojo API, sm100_structured output_writer): the
 // epilogue hands its finished output tile to a sink instead of storing it to the
@@ -8,7 +8,7 @@
 // (src_idx*top_k + src_topk)*msg_bytes + byte_off. "ep_signal_completion"
 // (shmem/ep_comm, ep_ord_r with has_rank_flag): per-expert count words are plain
 // stores made before an acquire-release election on a per-destination counter;
-// the producer elected last release-stores the rank flag.
+// the producer elected last publishes the rank flag.
 //
 // Design for sm_103a: one persistent CTA per SM walks a static schedule of
 // (expert, 128-row block, BN-column block) tiles. Warp 0 issues TMA loads of A and
@@ -18,9 +18,9 @@
 // accumulator with tcgen05.ld, round to bf16, stage 32 rows x 64 columns per warp
 // in shared memory and write each row's 128 contiguous bytes to its destination
 // with 16-byte stores (8 lanes per row). The double-buffered accumulator lets the
-// MMA of tile i+1 run while tile i is being sent. After the last row of a tile a
-// named barrier and one acquire-release increment count the tile; the CTA that
-// completes an expert's last tile runs the completion signalling.
+// MMA of tile i+1 run while tile i is being sent. After a barrier over the four
+// epilogue warps, the finished tile goes to warp 6, which counts tiles per expert
+// and runs the completion signalling, off the output path.
 //
 // Every wait is bounded (timeout_ns of %globaltimer): on expiry the kernel sets
 // EP_STATUS_TIMEOUT, the other roles stop at their next wait, outstanding TMA
@@ -29,6 +29,7 @@
 
 #include "ep_internal.h"
 #include "ep_ptx.cuh"
+#include "ep_sink.cuh"
 
 namespace ep {
 
@@ -44,92 +45,14 @@ struct GemmLayout {
     static constexpr int kOffStaging = kOffB + STAGES * kBBytes;
     static constexpr int kOffBars = kOffStaging + kEpiWarps * kWarpStaging;
     static constexpr int kNumBars = 2 * STAGES + 5;  // full, empty, acc_full x2, acc_empty x2, mma_done
-    static constexpr int kOffTmemSlot = kOffBars + kNumBars * 8;
-    static constexpr int kOffAbort = kOffTmemSlot + 4;
-    static constexpr int kOffPtrs = (kOffAbort + 4 + 15) / 16 * 16;  // 8 recv_buf + 8 recv_count
-    static constexpr int kOffTileStart = kOffPtrs + 16 * 8;
-    static constexpr int kOffExpertOff = kOffTileStart + 4 * (EP_MAX_LOCAL_EXPERTS + 1);
-    static constexpr int kQueue = 64;  // tile-completion queue, epilogue -> completion warp
-    static constexpr int kOffQueue = (kOffExpertOff + 4 * (EP_MAX_LOCAL_EXPERTS + 1) + 15) / 16 * 16;
-    static constexpr int kOffQueueCtl = kOffQueue + 16 * kQueue;  // head, tail, done
-    static constexpr int kEnd = kOffQueueCtl + 16;
+    static constexpr int kOffSink = (kOffBars + kNumBars * 8 + 15) / 16 * 16;
+    static constexpr int kEnd = kOffSink + static_cast<int>(sizeof(SinkShared));
     static constexpr int kSmemBytes = kEnd + 1024;  // slack to align the base to 1024
     static constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators
     static constexpr int kThreads = 224;            // TMA, MMA, 4 epilogue, completion
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM columns");
 };
-
-__device__ __forceinline__ void raise_abort(uint32_t *status, volatile int *abort_flag)
-{
-    atomicOr(status, EP_STATUS_TIMEOUT);
-    *abort_flag = 1;
-}
-
-// Completion signalling of local expert e towards every destination rank
-// ("ep_signal_completion", ep_ord_r with has_rank_flag). The caller has acquired
-// every row of expert e. For each destination: a plain progress store of the count
-// word, then the election on that destination's counter. The release half of the
-// acquire-release election is one system-scope fence ahead of all R increments
-// (it releases the rows and the count words); the acquire half is a second fence,
-// taken only when this call is elected for some destination, which also orders
-// the rank-flag stores after everything the other experts released.
-__device__ void signal_expert(const SendParams &p, int e, uint64_t *const *cnt)
-{
-    const int R = p.n_ranks;
-    for (int dst = 0; dst < R; ++dst) {
-        volatile uint64_t *w = cnt[dst] + static_cast<int64_t>(e) * R + p.my_rank;
-        *w = static_cast<uint64_t>(p.send_counts[e * R + dst]);
-    }
-    fence_acq_rel_sys();
-    int old[EP_MAX_RANKS];
-#pragma unroll
-    for (int dst = 0; dst < EP_MAX_RANKS; ++dst)
-        if (dst < R)
-            old[dst] = atom_add_relaxed_sys(&p.rank_counter[dst], 1);
-    bool elected = false;
-#pragma unroll
-    for (int dst = 0; dst < EP_MAX_RANKS; ++dst)
-        elected |= dst < R && old[dst] == p.El - 1;
-    if (!elected)
-        return;
-    fence_acq_rel_sys();
-#pragma unroll
-    for (int dst = 0; dst < EP_MAX_RANKS; ++dst) {
-        if (dst < R && old[dst] == p.El - 1) {
-            // last expert of this rank for dst: re-arm the counter for the next call and
-            // publish the whole rank through the rank flag
-            *reinterpret_cast<volatile int *>(&p.rank_counter[dst]) = 0;
-            st_relaxed_sys_u64(cnt[dst] + static_cast<int64_t>(p.El) * R + p.my_rank, p.epoch);
-        }
-    }
-}
-
-struct TileCoord {
-    int e, m_abs, m_end, nb;
-};
-
-__device__ __forceinline__ TileCoord decode_tile(int t, const int *tile_start, const int *eoff,
-                                                 int El, int n_blocks)
-{
-    // the largest expert whose first tile is <= t owns t (empty experts share starts)
-    int lo = 0, hi = El - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (tile_start[mid] <= t)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    TileCoord c;
-    c.e = lo;
-    const int local = t - tile_start[lo];
-    const int mt = local / n_blocks;
-    c.nb = local - mt * n_blocks;
-    c.m_abs = eoff[lo] + mt * BM;
-    c.m_end = eoff[lo + 1];
-    return c;
-}
 
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(224, 1)
@@ -149,16 +72,8 @@ __global__ void __launch_bounds__(224, 1)
     uint64_t *acc_full = bars + 2 * STAGES;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *mma_done = acc_empty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffTmemSlot);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffAbort);
-    uint8_t **s_recv = reinterpret_cast<uint8_t **>(smem + L::kOffPtrs);
-    uint64_t **s_cnt = reinterpret_cast<uint64_t **>(smem + L::kOffPtrs + 64);
-    int *s_tile_start = reinterpret_cast<int *>(smem + L::kOffTileStart);
-    int *s_eoff = reinterpret_cast<int *>(smem + L::kOffExpertOff);
-    int4 *s_queue = reinterpret_cast<int4 *>(smem + L::kOffQueue);
-    volatile int *q_head = reinterpret_cast<volatile int *>(smem + L::kOffQueueCtl);
-    volatile int *q_tail = q_head + 1;
-    volatile int *q_done = q_head + 2;
+    SinkShared *sh = reinterpret_cast<SinkShared *>(smem + L::kOffSink);
+    volatile int *abort_flag = &sh->abort_flag;
     const int El = p.El;
 
     // ---------------------------------------------------------------- prologue
@@ -172,41 +87,12 @@ __global__ void __launch_bounds__(224, 1)
             mbar_init(&acc_empty[a], L::kEpiWarps);
         }
         mbar_init(mma_done, 1);
-        *abort_flag = 0;
-        *q_head = 0;
-        *q_tail = 0;
-        *q_done = 0;
         fence_mbar_init();
     }
-    if (threadIdx.x < EP_MAX_RANKS) {
-        s_recv[threadIdx.x] = p.recv_buf[threadIdx.x];
-        s_cnt[threadIdx.x] = p.recv_count[threadIdx.x];
-    }
-    // expert row ranges: one load per thread, then one thread makes them monotone and
-    // clamped to the rows of A (so a malformed plan cannot send reads past the plan
-    // arrays) and builds the tile table
-    for (int e = threadIdx.x; e <= El; e += blockDim.x)
-        s_eoff[e] = __ldg(p.expert_offsets + e);
-    __syncthreads();
-    if (threadIdx.x == 32) {
-        int prev = 0;
-        for (int e = 0; e <= El; ++e) {
-            int v = s_eoff[e];
-            v = v < prev ? prev : v;
-            v = v > p.max_rows ? static_cast<int>(p.max_rows) : v;
-            s_eoff[e] = v;
-            prev = v;
-        }
-        int acc = 0;
-        for (int e = 0; e < El; ++e) {
-            s_tile_start[e] = acc;
-            acc += (s_eoff[e + 1] - s_eoff[e] + BM - 1) / BM * p.n_blocks;
-        }
-        s_tile_start[El] = acc;
-    }
+    sink_prologue(p, sh);
     if (warp == 1) {
         __syncwarp();
-        tmem_alloc(tmem_slot, L::kTmemCols);
+        tmem_alloc(&sh->tmem_slot, L::kTmemCols);
         tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
@@ -216,8 +102,8 @@ __global__ void __launch_bounds__(224, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
-    const int total_tiles = s_tile_start[El];
+    const uint32_t tmem_base = sh->tmem_slot;
+    const int total_tiles = sh->tile_start[El];
 
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
@@ -227,7 +113,7 @@ __global__ void __launch_bounds__(224, 1)
             uint32_t used_mask = 0, last_parity = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-                const TileCoord c = decode_tile(t, s_tile_start, s_eoff, El, p.n_blocks);
+                const TileCoord c = decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks);
                 const int w_row = c.e * p.N + c.nb * BN;
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag)) {
@@ -310,43 +196,19 @@ __global__ void __launch_bounds__(224, 1)
         const int q = warp & 3;  // TMEM lane quarter this warp may read
         const int epi_tid = threadIdx.x - 64;
         const uint32_t stg = smem_u32(smem + L::kOffStaging + (warp - 2) * L::kWarpStaging);
-        const int R = p.n_ranks;
-
-        uint64_t *trace = nullptr;  // this block's trace words (thread epi_tid 0 only)
-        if (p.trace && epi_tid == 0) {
-            trace = p.trace + static_cast<int64_t>(blockIdx.x) * (2 + 4 * p.trace_records);
+        uint64_t *trace = epi_tid == 0 ? trace_block(p) : nullptr;
+        if (trace)
             trace[1] = globaltimer_ns();
-        }
+
         bool ok = true;
         bool push_ok = true;  // epi_tid 0: the last hand-off to the completion warp succeeded
         int i = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++i) {
-            const TileCoord c = decode_tile(t, s_tile_start, s_eoff, El, p.n_blocks);
+            const TileCoord c = decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks);
             const int as = i & 1;
             const uint32_t aphase = (i >> 1) & 1;
-
             // resolve this thread's row destination while the MMA runs
-            const int m = c.m_abs + q * 32 + lane;
-            uint8_t *row_base = nullptr;
-            if (m < c.m_end) {
-                if (p.sink_enabled) {
-                    const int *seg = p.seg_offsets + c.e * (R + 1);
-                    int dst = -1;
-                    for (int rk = 0; rk < R; ++rk)
-                        if (m >= __ldg(seg + rk) && m < __ldg(seg + rk + 1))
-                            dst = rk;
-                    const int2 si = __ldg(reinterpret_cast<const int2 *>(p.src_info) + m);
-                    if (dst < 0 || si.x < 0 || si.x >= p.max_tokens || si.y < 0 ||
-                        si.y >= p.top_k) {
-                        atomicOr(p.status, EP_STATUS_BOUNDS);
-                    } else {
-                        row_base = s_recv[dst] +
-                                   (static_cast<int64_t>(si.x) * p.top_k + si.y) * p.msg_bytes;
-                    }
-                } else {
-                    row_base = p.C + static_cast<int64_t>(m) * p.N * 2;
-                }
-            }
+            uint8_t *row_base = resolve_row(p, sh, c, c.m_abs + q * 32 + lane);
 
             ok = mbar_wait(&acc_full[as], aphase, p.timeout_ns, abort_flag) && push_ok;
             // all four epilogue warps take the same decision, so none is left waiting
@@ -406,27 +268,14 @@ __global__ void __launch_bounds__(224, 1)
 
             if (p.sink_enabled) {
                 // all 128 sink threads' stores of this tile precede the hand-off to the
-                // completion warp, which counts the tile
+                // completion warp, which counts the tile; a failed hand-off is voted
+                // on at the next tile (or reported after the loop)
                 named_bar_sync(1, 128);
                 if (epi_tid == 0) {
                     if (rec)
                         rec[2] = globaltimer_ns();
-                    const int tiles_e = (c.m_end - s_eoff[c.e] + BM - 1) / BM * p.n_blocks;
-                    // bounded wait for a free queue slot; a failure is voted on at the
-                    // next tile (or reported after the loop)
-                    const uint64_t t0 = globaltimer_ns();
-                    while (*q_tail - *q_head >= L::kQueue) {
-                        if (*abort_flag || globaltimer_ns() - t0 > p.timeout_ns) {
-                            push_ok = false;
-                            break;
-                        }
-                    }
-                    if (push_ok) {
-                        const int tl = *q_tail;
-                        s_queue[tl % L::kQueue] = make_int4(c.e, rec ? i : -1, tiles_e, 0);
-                        __threadfence_block();
-                        *q_tail = tl + 1;
-                    }
+                    const int tiles_e = (c.m_end - sh->eoff[c.e] + BM - 1) / BM * p.n_blocks;
+                    push_ok = push_tile_done(p, sh, c.e, rec ? i : -1, tiles_e);
                 }
             } else if (rec) {
                 rec[2] = rec[3] = globaltimer_ns();
@@ -435,79 +284,16 @@ __global__ void __launch_bounds__(224, 1)
         if (epi_tid == 0) {
             if (trace)
                 trace[0] = static_cast<uint64_t>(i);
-            __threadfence_block();
-            *q_done = 1;
+            close_queue(sh);
             if (!push_ok)
                 raise_abort(p.status, abort_flag);
         }
         if (!ok && lane == 0)
             raise_abort(p.status, abort_flag);
-    } else if (warp == 6) {
+    } else {
         // ------------------------------------------- completion counting + signalling
-        // Runs beside the epilogue so that neither the per-tile release fence nor the
-        // system-scope signalling ever stalls the output path.
-        if (lane == 0 && p.sink_enabled) {
-            uint64_t *trace =
-                p.trace ? p.trace + static_cast<int64_t>(blockIdx.x) * (2 + 4 * p.trace_records)
-                        : nullptr;
-            if (blockIdx.x == 0) {
-                // experts without rows have no tile to complete: signal their zero counts
-                for (int e = 0; e < El; ++e)
-                    if (s_eoff[e + 1] == s_eoff[e])
-                        signal_expert(p, e, s_cnt);
-            }
-            int head = 0;
-            uint64_t t0 = globaltimer_ns();
-            while (true) {
-                const int tail = *q_tail;
-                if (head < tail) {
-                    __threadfence_block();
-                    int4 ent[8];
-                    int n = 0;
-                    while (head < tail && n < 8)
-                        ent[n++] = s_queue[(head++) % L::kQueue];
-                    __threadfence_block();
-                    *q_head = head;
-                    // one release fence covers the rows of every tile popped here
-                    fence_acq_rel_gpu();
-                    bool last[8];
-                    bool any = false;
-                    for (int j = 0; j < n; ++j) {
-                        const int old = atom_add_relaxed_gpu(&p.atomic_counter[ent[j].x], 1);
-                        last[j] = old == ent[j].z - 1;
-                        any |= last[j];
-                    }
-                    if (any)
-                        fence_acq_rel_gpu();  // acquire the expert's other tiles
-                    for (int j = 0; j < n; ++j) {
-                        if (last[j]) {
-                            *reinterpret_cast<volatile int *>(&p.atomic_counter[ent[j].x]) = 0;
-                            signal_expert(p, ent[j].x, s_cnt);
-                        }
-                        if (trace && ent[j].y >= 0) {
-                            uint64_t *rec = trace + 2 + 4 * ent[j].y;
-                            if (last[j])
-                                rec[0] |= 1ull << 63;
-                            rec[3] = globaltimer_ns();
-                        }
-                    }
-                    t0 = globaltimer_ns();
-                    continue;
-                }
-                if (*q_done) {
-                    __threadfence_block();
-                    if (*q_tail == head)
-                        break;
-                    continue;
-                }
-                if (*abort_flag)
-                    break;
-                if (globaltimer_ns() - t0 > p.timeout_ns) {
-                    raise_abort(p.status, abort_flag);
-                    break;
-                }
-            }
-        }
+        if (lane == 0 && p.sink_enabled)
+            completion_loop(p, sh);
         __syncwarp();
     }
 

@@ -1,0 +1,346 @@
+// Grouped expert GEMM with blockwise fp8 operands (the "blockwise_fp8_1d2d"
+// family named in the "P3PeerSendConfig" description: 1x128 activation scales,
+// 128x128 weight scales), with the same fused EP-combine send as the bf16 kernel.
+//
+// y[m, n] = sum_kb sa[m, kb] * sw[e, n/128, kb] * sum_{k in kb} a8[m, k] * w8[n, k]
+//
+// The scales are arbitrary fp32 values, so they cannot ride on the tensor cores'
+// power-of-two block scaling: every 128-wide K block is its own fp32 partial sum
+// on the tensor cores, and warps outside the MMA path scale and accumulate the
+// partials ("promotion") in registers.
+//
+// Design for sm_103a, one persistent CTA per SM, 352 threads:
+//  warp 0     TMA: A box 128 (K bytes) x 128 rows, W box 128 x 256, 128-byte swizzle,
+//             4-stage ring; one stage is exactly one scale block.
+//  warp 1     TMEM (512 columns = two 128 x 256 fp32 partial buffers) and the MMA:
+//             tcgen05.mma kind::f8f6f4, e4m3 x e4m3, M 128, N 256, K 32 per
+//             instruction; one partial per K block, alternating buffers.
+//  warp 2     completion counting + signalling (shared with the bf16 kernel).
+//  warps 3-10 promotion + epilogue: warp w reads TMEM lane quarter w % 4 and column
+//             half (w - 3) / 4; each thread keeps its row's 128 fp32 accumulators,
+//             adds sa[m, kb] * sw[e, n/128, kb] * partial per K block, then rounds to
+//             bf16 and sends the row in 64-byte pieces (4 lanes per row).
+#include <cuda_bf16.h>
+
+#include "ep_internal.h"
+#include "ep_ptx.cuh"
+#include "ep_sink.cuh"
+
+namespace ep {
+
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+struct Fp8Layout {
+    static constexpr int BN = 256;
+    static constexpr int STAGES = 4;
+    static constexpr int kABytes = BM * kRowBytesK;  // 128 rows x 128 e4m3
+    static constexpr int kBBytes = BN * kRowBytesK;  // 256 rows x 128 e4m3
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kPromoWarps = 8;
+    static constexpr int kStgRow = 80;                     // 64 data bytes + 16 pad
+    static constexpr int kWarpStaging = 32 * kStgRow;      // 32 rows x 32 bf16 columns
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + STAGES * kABytes;
+    static constexpr int kOffStaging = kOffB + STAGES * kBBytes;
+    static constexpr int kOffBars = kOffStaging + kPromoWarps * kWarpStaging;
+    static constexpr int kNumBars = 2 * STAGES + 5;  // full, empty, pfull x2, pfree x2, mma_done
+    static constexpr int kOffSink = (kOffBars + kNumBars * 8 + 15) / 16 * 16;
+    static constexpr int kEnd = kOffSink + static_cast<int>(sizeof(SinkShared));
+    static constexpr int kSmemBytes = kEnd + 1024;
+    static constexpr uint32_t kTmemCols = 2 * BN;
+    static constexpr int kThreads = 32 * (3 + kPromoWarps);
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+__global__ void __launch_bounds__(352, 1)
+    gemm_send_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                         const __grid_constant__ CUtensorMap tmap_b,
+                         const __grid_constant__ SendParams p)
+{
+    using L = Fp8Layout;
+    constexpr int BN = L::BN;
+    constexpr int STAGES = L::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBars);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES;
+    uint64_t *pfull = bars + 2 * STAGES;
+    uint64_t *pfree = pfull + 2;
+    uint64_t *mma_done = pfree + 2;
+    SinkShared *sh = reinterpret_cast<SinkShared *>(smem + L::kOffSink);
+    volatile int *abort_flag = &sh->abort_flag;
+    const int El = p.El;
+    const int nkb = p.num_k_blocks;  // K / 128: one scale block per K block
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&pfull[b], 1);
+            mbar_init(&pfree[b], L::kPromoWarps);
+        }
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+    }
+    sink_prologue(p, sh);
+    if (warp == 1) {
+        __syncwarp();
+        tmem_alloc(&sh->tmem_slot, L::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmap_a);
+        tma_prefetch_map(&tmap_b);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = sh->tmem_slot;
+    const int total_tiles = sh->tile_start[El];
+
+    if (warp == 0) {
+        // ------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t used_mask = 0, last_parity = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+                const TileCoord c = decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks);
+                const int w_row = c.e * p.N + c.nb * BN;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
+                    tma_load_2d(smem + L::kOffA + stage * L::kABytes, &tmap_a, &full[stage],
+                                kb * 128, c.m_abs);
+                    tma_load_2d(smem + L::kOffB + stage * L::kBBytes, &tmap_b, &full[stage],
+                                kb * 128, w_row);
+                    used_mask |= 1u << stage;
+                    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok)
+                raise_abort(p.status, abort_flag);
+            volatile int no_abort = 0;
+            for (int s = 0; s < STAGES; ++s)
+                if (used_mask & (1u << s))
+                    mbar_wait(&full[s], (last_parity >> s) & 1u, p.timeout_ns, &no_abort);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ----------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(0u, BM, BN);  // e4m3 x e4m3 -> fp32
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t g = 0;  // K blocks issued so far (selects the partial buffer)
+            bool ok = true;
+            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+                for (int kb = 0; kb < nkb; ++kb, ++g) {
+                    const uint32_t pb = g & 1u, pph = (g >> 1) & 1u;
+                    if (!mbar_wait(&pfree[pb], pph ^ 1u, p.timeout_ns, abort_flag) ||
+                        !mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + L::kOffA + stage * L::kABytes);
+                    const uint32_t b_addr = smem_u32(smem + L::kOffB + stage * L::kBBytes);
+                    const uint32_t d_tmem = tmem_base + pb * BN;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f8(d_tmem, desc_kmajor_sw128(a_addr + kk * 32),
+                               desc_kmajor_sw128(b_addr + kk * 32), idesc, kk != 0 ? 1u : 0u);
+                    mma_commit(&empty[stage]);
+                    mma_commit(&pfull[pb]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok)
+                raise_abort(p.status, abort_flag);
+            mma_commit(mma_done);
+            volatile int no_abort = 0;
+            mbar_wait(mma_done, 0, p.timeout_ns, &no_abort);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------- completion counting + signalling
+        if (lane == 0 && p.sink_enabled)
+            completion_loop(p, sh);
+        __syncwarp();
+    } else {
+        // --------------------------------------------- promotion + epilogue + sink
+        const int q = warp & 3;          // TMEM lane quarter
+        const int half = (warp - 3) >> 2;  // column half of the 256-wide tile
+        const int ptid = threadIdx.x - 96;  // 0..255
+        const uint32_t stg = smem_u32(smem + L::kOffStaging + (warp - 3) * L::kWarpStaging);
+        const int row = q * 32 + lane;
+        const int n_scale_blocks = p.N / 128;
+        uint64_t *trace = ptid == 0 ? trace_block(p) : nullptr;
+        if (trace)
+            trace[1] = globaltimer_ns();
+
+        bool ok = true;
+        bool push_ok = true;
+        uint32_t g = 0;
+        int i = 0;
+        for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++i) {
+            const TileCoord c = decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks);
+            const int m = c.m_abs + row;
+            uint8_t *row_base = resolve_row(p, sh, c, m);
+            // scale rows (rows past the tile's group read the last row's scales: unused)
+            const int m_s = m < p.max_rows ? m : static_cast<int>(p.max_rows) - 1;
+            const float *sa = p.a_scales + static_cast<int64_t>(m_s) * nkb;
+            const float *sw = p.w_scales +
+                              (static_cast<int64_t>(c.e) * n_scale_blocks +
+                               (c.nb * BN + half * 128) / 128) * nkb;
+            float acc[128];
+#pragma unroll
+            for (int j = 0; j < 128; ++j)
+                acc[j] = 0.f;
+            float sa_next = __ldg(sa), sw_next = __ldg(sw);
+            bool ok_t = push_ok;
+            for (int kb = 0; kb < nkb && ok_t; ++kb, ++g) {
+                const float s = sa_next * sw_next;
+                if (kb + 1 < nkb) {
+                    sa_next = __ldg(sa + kb + 1);
+                    sw_next = __ldg(sw + kb + 1);
+                }
+                const uint32_t pb = g & 1u, pph = (g >> 1) & 1u;
+                ok_t = mbar_wait(&pfull[pb], pph, p.timeout_ns, abort_flag);
+                ok_t = __all_sync(0xffffffffu, ok_t);
+                if (!ok_t)
+                    break;
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       pb * BN + half * 128;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t v0[16], v1[16];
+                    tmem_ld_32x32b_x16(taddr + c4 * 32, v0);
+                    tmem_ld_32x32b_x16(taddr + c4 * 32 + 16, v1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        acc[c4 * 32 + j] = fmaf(s, __uint_as_float(v0[j]), acc[c4 * 32 + j]);
+                        acc[c4 * 32 + 16 + j] =
+                            fmaf(s, __uint_as_float(v1[j]), acc[c4 * 32 + 16 + j]);
+                    }
+                }
+                // partial read: hand the buffer back to the MMA warp
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&pfree[pb]);
+            }
+            ok = named_bar_and(2, 256, ok_t);
+            if (!ok)
+                break;
+            uint64_t *rec = (trace && i < p.trace_records) ? trace + 2 + 4 * i : nullptr;
+            if (rec) {
+                rec[0] = static_cast<uint64_t>(t) | (static_cast<uint64_t>(c.e) << 32);
+                rec[1] = globaltimer_ns();
+            }
+
+            // bf16 rows, 32 columns at a time: stage, then 4 lanes per row send 64 bytes
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        __nv_bfloat162 b = __float22bfloat162_rn(
+                            make_float2(acc[c4 * 32 + ch * 8 + 2 * h],
+                                        acc[c4 * 32 + ch * 8 + 2 * h + 1]));
+                        w[h] = *reinterpret_cast<uint32_t *>(&b);
+                    }
+                    st_shared_v4(stg + lane * L::kStgRow + ch * 16,
+                                 make_uint4(w[0], w[1], w[2], w[3]));
+                }
+                __syncwarp();
+                const int col_byte = (c.nb * BN + half * 128 + c4 * 32) * 2;
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const int r = it * 8 + (lane >> 2);
+                    const int ch = lane & 3;
+                    const unsigned long long base = __shfl_sync(
+                        0xffffffffu, reinterpret_cast<unsigned long long>(row_base), r);
+                    const uint4 val = ld_shared_v4(stg + r * L::kStgRow + ch * 16);
+                    if (base != 0ull)
+                        st_global_v4(reinterpret_cast<uint8_t *>(base) + col_byte + ch * 16, val);
+                }
+                __syncwarp();
+            }
+
+            if (p.sink_enabled) {
+                named_bar_sync(1, 256);
+                if (ptid == 0) {
+                    if (rec)
+                        rec[2] = globaltimer_ns();
+                    const int tiles_e = (c.m_end - sh->eoff[c.e] + BM - 1) / BM * p.n_blocks;
+                    push_ok = push_tile_done(p, sh, c.e, rec ? i : -1, tiles_e);
+                }
+            } else if (rec) {
+                rec[2] = rec[3] = globaltimer_ns();
+            }
+        }
+        if (ptid == 0) {
+            if (trace)
+                trace[0] = static_cast<uint64_t>(i);
+            close_queue(sh);
+            if (!push_ok)
+                raise_abort(p.status, abort_flag);
+        }
+        if (!ok && lane == 0)
+            raise_abort(p.status, abort_flag);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, L::kTmemCols);
+    }
+}
+
+cudaError_t launch_gemm_send_fp8(const CUtensorMap &ta, const CUtensorMap &tb,
+                                 const SendParams &p, int grid, cudaStream_t s)
+{
+    using L = Fp8Layout;
+    cudaError_t err = cudaFuncSetAttribute(gemm_send_fp8_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           L::kSmemBytes);
+    if (err != cudaSuccess)
+        return err;
+    gemm_send_fp8_kernel<<<grid, L::kThreads, L::kSmemBytes, s>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

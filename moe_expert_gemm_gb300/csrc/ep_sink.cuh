@@ -1,0 +1,272 @@
+// The sink side of the fused expert GEMM, shared by the bf16 and fp8 kernels:
+// tile schedule, per-row destination resolution, the hand-off of finished tiles
+// to a completion warp, and the completion signalling.
+//
+// "EpiloguePeerSink": the finished output tile goes to the peers that own its rows
+// instead of to the local C; rows m_abs <= m < m_end of the tile's group.
+// "P3PeerSendConfig": row (src_idx, src_topk) lands at
+// (src_idx*top_k + src_topk)*msg_bytes + byte_off of its rank's receive buffer; the
+// count of expert e from rank rk sits at e*n_ranks + rk.
+// "ep_signal_completion" (ep_ord_r, has_rank_flag): plain count stores before an
+// acquire-release election on a per-destination counter bounded by the local
+// expert count; the elected producer publishes the rank flag in the buffer tail.
+#pragma once
+
+#include "ep_internal.h"
+#include "ep_ptx.cuh"
+
+namespace ep {
+
+constexpr int kQueue = 64;  // finished-tile queue, epilogue -> completion warp
+
+// Shared-memory state of the sink, one per thread block.
+struct SinkShared {
+    uint8_t *recv[EP_MAX_RANKS];
+    uint64_t *cnt[EP_MAX_RANKS];
+    int tile_start[EP_MAX_LOCAL_EXPERTS + 1];
+    int eoff[EP_MAX_LOCAL_EXPERTS + 1];
+    int4 queue[kQueue];  // {expert, trace record or -1, tiles of the expert, 0}
+    int q_head, q_tail, q_done, abort_flag;
+    uint32_t tmem_slot;
+};
+
+__device__ __forceinline__ void raise_abort(uint32_t *status, volatile int *abort_flag)
+{
+    atomicOr(status, EP_STATUS_TIMEOUT);
+    *abort_flag = 1;
+}
+
+// Completion signalling of local expert e towards every destination rank. The
+// caller has acquired every row of expert e. For each destination: a plain
+// progress store of the count word, then the election on that destination's
+// counter. The release half of the acquire-release election is one system-scope
+// fence ahead of all R increments (it releases the rows and the count words); the
+// acquire half is a second fence, taken only when this call is elected for some
+// destination, which also orders the rank-flag stores after everything the other
+// experts released.
+static __device__ __noinline__ void signal_expert(const SendParams &p, int e, uint64_t *const *cnt)
+{
+    const int R = p.n_ranks;
+    for (int dst = 0; dst < R; ++dst) {
+        volatile uint64_t *w = cnt[dst] + static_cast<int64_t>(e) * R + p.my_rank;
+        *w = static_cast<uint64_t>(p.send_counts[e * R + dst]);
+    }
+    fence_acq_rel_sys();
+    int old[EP_MAX_RANKS];
+#pragma unroll
+    for (int dst = 0; dst < EP_MAX_RANKS; ++dst)
+        if (dst < R)
+            old[dst] = atom_add_relaxed_sys(&p.rank_counter[dst], 1);
+    bool elected = false;
+#pragma unroll
+    for (int dst = 0; dst < EP_MAX_RANKS; ++dst)
+        elected |= dst < R && old[dst] == p.El - 1;
+    if (!elected)
+        return;
+    fence_acq_rel_sys();
+#pragma unroll
+    for (int dst = 0; dst < EP_MAX_RANKS; ++dst) {
+        if (dst < R && old[dst] == p.El - 1) {
+            // last expert of this rank for dst: re-arm the counter for the next call and
+            // publish the whole rank through the rank flag
+            *reinterpret_cast<volatile int *>(&p.rank_counter[dst]) = 0;
+            st_relaxed_sys_u64(cnt[dst] + static_cast<int64_t>(p.El) * R + p.my_rank, p.epoch);
+        }
+    }
+}
+
+struct TileCoord {
+    int e, m_abs, m_end, nb;
+};
+
+// Tiles are numbered expert by expert; within an expert, row block by row block,
+// column block fastest (concurrent blocks share the A rows and sweep W).
+__device__ __forceinline__ TileCoord decode_tile(int t, const int *tile_start, const int *eoff,
+                                                 int El, int n_blocks)
+{
+    // the largest expert whose first tile is <= t owns t (empty experts share starts)
+    int lo = 0, hi = El - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tile_start[mid] <= t)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    TileCoord c;
+    c.e = lo;
+    const int local = t - tile_start[lo];
+    const int mt = local / n_blocks;
+    c.nb = local - mt * n_blocks;
+    c.m_abs = eoff[lo] + mt * BM;
+    c.m_end = eoff[lo + 1];
+    return c;
+}
+
+// Called by every thread of the block: destination pointers, expert row ranges
+// (made monotone and clamped to the rows of A so that a malformed plan cannot send
+// reads past the plan arrays) and the tile table. Ends with __syncthreads.
+__device__ __forceinline__ void sink_prologue(const SendParams &p, SinkShared *sh)
+{
+    const int El = p.El;
+    if (threadIdx.x < EP_MAX_RANKS) {
+        sh->recv[threadIdx.x] = p.recv_buf[threadIdx.x];
+        sh->cnt[threadIdx.x] = p.recv_count[threadIdx.x];
+    }
+    if (threadIdx.x == 0) {
+        sh->q_head = 0;
+        sh->q_tail = 0;
+        sh->q_done = 0;
+        sh->abort_flag = 0;
+    }
+    for (int e = threadIdx.x; e <= El; e += blockDim.x)
+        sh->eoff[e] = __ldg(p.expert_offsets + e);
+    __syncthreads();
+    if (threadIdx.x == 32) {
+        int prev = 0;
+        for (int e = 0; e <= El; ++e) {
+            int v = sh->eoff[e];
+            v = v < prev ? prev : v;
+            v = v > p.max_rows ? static_cast<int>(p.max_rows) : v;
+            sh->eoff[e] = v;
+            prev = v;
+        }
+        int acc = 0;
+        for (int e = 0; e < El; ++e) {
+            sh->tile_start[e] = acc;
+            acc += (sh->eoff[e + 1] - sh->eoff[e] + BM - 1) / BM * p.n_blocks;
+        }
+        sh->tile_start[El] = acc;
+    }
+    __syncthreads();
+}
+
+// Destination of row m of tile c: its slot in the receive buffer of the rank that
+// owns its token (sink on), or its row of the local C (sink off). nullptr when the
+// row lies past the group (m >= m_end) or its destination is outside the buffer
+// (then EP_STATUS_BOUNDS is raised and the row is skipped).
+__device__ __forceinline__ uint8_t *resolve_row(const SendParams &p, const SinkShared *sh,
+                                                const TileCoord &c, int m)
+{
+    if (m >= c.m_end)
+        return nullptr;
+    if (!p.sink_enabled)
+        return p.C + static_cast<int64_t>(m) * p.N * 2;
+    const int R = p.n_ranks;
+    const int *seg = p.seg_offsets + c.e * (R + 1);
+    int dst = -1;
+    for (int rk = 0; rk < R; ++rk)
+        if (m >= __ldg(seg + rk) && m < __ldg(seg + rk + 1))
+            dst = rk;
+    const int2 si = __ldg(reinterpret_cast<const int2 *>(p.src_info) + m);
+    if (dst < 0 || si.x < 0 || si.x >= p.max_tokens || si.y < 0 || si.y >= p.top_k) {
+        atomicOr(p.status, EP_STATUS_BOUNDS);
+        return nullptr;
+    }
+    return sh->recv[dst] + (static_cast<int64_t>(si.x) * p.top_k + si.y) * p.msg_bytes;
+}
+
+__device__ __forceinline__ uint64_t *trace_block(const SendParams &p)
+{
+    return p.trace ? p.trace + static_cast<int64_t>(blockIdx.x) * (2 + 4 * p.trace_records)
+                   : nullptr;
+}
+
+// One epilogue thread hands a finished tile (all of whose rows have been stored,
+// as ordered by a barrier over the epilogue threads) to the completion warp.
+// Bounded wait for a free slot; false when it gave up.
+__device__ __forceinline__ bool push_tile_done(const SendParams &p, SinkShared *sh, int e,
+                                               int record, int tiles_e)
+{
+    volatile int *head = &sh->q_head;
+    volatile int *tail = &sh->q_tail;
+    volatile int *abort_flag = &sh->abort_flag;
+    const uint64_t t0 = globaltimer_ns();
+    while (*tail - *head >= kQueue) {
+        if (*abort_flag || globaltimer_ns() - t0 > p.timeout_ns)
+            return false;
+    }
+    const int tl = *tail;
+    sh->queue[tl % kQueue] = make_int4(e, record, tiles_e, 0);
+    __threadfence_block();
+    *tail = tl + 1;
+    return true;
+}
+
+// The epilogue has no more tiles (or gave up).
+__device__ __forceinline__ void close_queue(SinkShared *sh)
+{
+    __threadfence_block();
+    *reinterpret_cast<volatile int *>(&sh->q_done) = 1;
+}
+
+// Completion warp, one thread: counts finished tiles per expert (one gpu-scope
+// release fence per batch of tiles, acquire fence when an expert completes) and
+// runs the signalling of every expert this block completes. Block 0 also
+// signals the experts without rows, which have no tile to complete.
+static __device__ void completion_loop(const SendParams &p, SinkShared *sh)
+{
+    volatile int *head_p = &sh->q_head;
+    volatile int *tail_p = &sh->q_tail;
+    volatile int *done_p = &sh->q_done;
+    volatile int *abort_flag = &sh->abort_flag;
+    uint64_t *trace = trace_block(p);
+    if (blockIdx.x == 0) {
+        for (int e = 0; e < p.El; ++e)
+            if (sh->eoff[e + 1] == sh->eoff[e])
+                signal_expert(p, e, sh->cnt);
+    }
+    int head = 0;
+    uint64_t t0 = globaltimer_ns();
+    while (true) {
+        const int tail = *tail_p;
+        if (head < tail) {
+            __threadfence_block();
+            int4 ent[8];
+            int n = 0;
+            while (head < tail && n < 8)
+                ent[n++] = sh->queue[(head++) % kQueue];
+            __threadfence_block();
+            *head_p = head;
+            // one release fence covers the rows of every tile popped here
+            fence_acq_rel_gpu();
+            bool last[8];
+            bool any = false;
+            for (int j = 0; j < n; ++j) {
+                const int old = atom_add_relaxed_gpu(&p.atomic_counter[ent[j].x], 1);
+                last[j] = old == ent[j].z - 1;
+                any |= last[j];
+            }
+            if (any)
+                fence_acq_rel_gpu();  // acquire the expert's other tiles
+            for (int j = 0; j < n; ++j) {
+                if (last[j]) {
+                    *reinterpret_cast<volatile int *>(&p.atomic_counter[ent[j].x]) = 0;
+                    signal_expert(p, ent[j].x, sh->cnt);
+                }
+                if (trace && ent[j].y >= 0) {
+                    uint64_t *rec = trace + 2 + 4 * ent[j].y;
+                    if (last[j])
+                        rec[0] |= 1ull << 63;
+                    rec[3] = globaltimer_ns();
+                }
+            }
+            t0 = globaltimer_ns();
+            continue;
+        }
+        if (*done_p) {
+            __threadfence_block();
+            if (*tail_p == head)
+                break;
+            continue;
+        }
+        if (*abort_flag)
+            break;
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+            raise_abort(p.status, abort_flag);
+            break;
+        }
+    }
+}
+
+}  // namespace ep

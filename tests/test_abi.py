@@ -92,6 +92,15 @@ def test_unaligned_operand_rejected(lib):
         ep.EP_ERR_INVALID_ARG
 
 
+def test_fp8_shape_rules(lib):
+    """Blockwise fp8 needs whole 128-wide scale blocks along K and 256-column tiles."""
+    a = ep.ep_send_args()
+    for kw in (dict(K=192), dict(N=384, msg_bytes=768)):
+        cfg = _cfg(dtype=ep.EP_FP8_1D2D, **kw)
+        assert lib.grouped_gemm_combine_send(ctypes.byref(cfg), ctypes.byref(a), None) == \
+            ep.EP_ERR_UNSUPPORTED
+
+
 def test_strerror(lib):
     assert ep.ep_strerror(ep.EP_ERR_UNSUPPORTED) == "unsupported configuration"
     assert "timed out" in ep.ep_strerror(ep.EP_STATUS_TIMEOUT)

@@ -17,7 +17,8 @@ from synth import WORKLOADS
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name", ["mixtral_prefill", "dsv3_decode", "qwen3_skew"])
+@pytest.mark.parametrize("name", ["mixtral_prefill", "dsv3_decode", "qwen3_skew",
+                                  "dsv3_prefill_fp8"])
 def test_full_size_sampled_parity(name):
     w = WORKLOADS[name]
     R, El, k, T, N = w.n_ranks, w.n_local_experts, w.top_k, w.tokens, w.N

@@ -88,6 +88,13 @@ EDGE = [
                                "softmax_sel", 47), "empty"),
     ("qwen_shape_small", Workload("qwen_small", 8, 16, 8, 48, 1536, 4096, "bf16", "zipf",
                                   "softmax_sel", 48), "random"),
+    # blockwise fp8: several scale blocks along K and N, ragged tails, empty experts
+    ("fp8_small", Workload("fp8_small", 4, 4, 2, 100, 384, 512, "fp8_1d2d", "uniform",
+                           "sigmoid_sel", 51), "random"),
+    ("fp8_zipf_empty", Workload("fp8_zipf", 4, 4, 4, 90, 256, 256, "fp8_1d2d", "zipf",
+                                "sigmoid_sel", 52), "random"),
+    ("fp8_dsv3_shape_small", Workload("fp8_dsv3_small", 8, 32, 8, 64, 2048, 7168, "fp8_1d2d",
+                                      "uniform", "sigmoid_sel", 53), "random"),
 ]
 
 
