@@ -63,6 +63,11 @@ def parse_args():
                     help="target host time of the CPU-baseline sample")
     ap.add_argument("--trace", default=None,
                     help="after timing, run one traced send and write its summary here")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override tokens per rank (profiling a smaller case of a workload)")
+    ap.add_argument("--solo", action="store_true",
+                    help="profiling aid: only the timed rank's operands, no peer staging, and "
+                         "the step is the fused send alone (no combine, no e2e, no baseline)")
     return ap.parse_args()
 
 
@@ -263,20 +268,24 @@ def main():
     ep.load()
 
     w = WORKLOADS[args.workload]
+    if args.tokens:
+        import dataclasses
+        w = dataclasses.replace(w, tokens=args.tokens, name=f"{w.name}@T{args.tokens}")
     q = rank % w.n_ranks  # the logical rank this process plays
     routing = make_routing(w)
     rows = rows_per_rank(w, routing.topk_ids)
-    values = [make_rank_values(w, r, int(rows[r])) for r in range(w.n_ranks)]
+    ranks = [q] if args.solo else list(range(w.n_ranks))
+    values = {r: make_rank_values(w, r, int(rows[r])) for r in ranks}
 
     s = EpSystem(w.n_ranks, w.n_local_experts, w.top_k, w.tokens, w.K, w.N, w.dtype)
     s.set_routing(routing.topk_ids)
-    for r in range(w.n_ranks):
+    for r in ranks:
         s.plan(r)
         v = values[r]
         s.set_operands(r, v["A"], v["W"], v.get("a_scales"), v.get("w_scales"))
     s.set_gates(q, routing.gates[q])
     # peers' rows land in every receive buffer once (their producers are not timed)
-    for r in range(w.n_ranks):
+    for r in ranks:
         s.send(r, epoch=1)
     torch.cuda.synchronize()
     st = s.status_words()
@@ -307,7 +316,8 @@ def main():
         s.send(q, e, stream)
         if evs is not None:
             evs[1].record(stream)
-        s.combine(q, e, stream)
+        if not args.solo:
+            s.combine(q, e, stream)
         if evs is not None:
             evs[2].record(stream)
 
@@ -340,14 +350,15 @@ def main():
         epoch[0] += 1
         s.counts[q].index_fill_(0, peer_idx, e)
         tr = s.send_traced(q, e, records=256)
-        s.combine(q, e, stream)
+        if not args.solo:
+            s.combine(q, e, stream)
         torch.cuda.synchronize()
         with open(args.trace, "w") as f:
             json.dump({"workload": w.name, "summary": summarize_trace(tr), "blocks": tr}, f)
 
     # ------------------------------------------------------ end to end (host buffers)
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.solo:
         A_dev = s.ops[q]["A"]
         A_host = A_dev.cpu().pin_memory()
         g_host = s.gates[q].cpu().pin_memory()
@@ -442,7 +453,9 @@ def main():
     }
     if e2e is not None:
         line["e2e"] = e2e
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if args.solo:
+        line["config"]["solo"] = "profiling aid: fused send only, peers not staged"
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.solo:
         import oracle
         plans = {r: oracle.plan(w.n_ranks, w.n_local_experts, w.top_k, routing.topk_ids, r)
                  for r in range(w.n_ranks)}

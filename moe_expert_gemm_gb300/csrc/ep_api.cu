@@ -95,6 +95,13 @@ int check_config(const ep_config *c)
     return EP_OK;
 }
 
+// Column tile of the fp8 kernel: 256 where N allows it (half the operand traffic per
+// FLOP of a 128-wide tile, two fp32 partial buffers in TMEM), else 128 (four buffers).
+int fp8_tile_n(int N)
+{
+    return N % 256 == 0 ? 256 : 128;
+}
+
 int cuda_status(cudaError_t e)
 {
     return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
@@ -159,9 +166,8 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
         return EP_ERR_UNSUPPORTED;
     if (!fp8 && (cfg->K % 64 != 0 || cfg->N % 64 != 0))
         return EP_ERR_UNSUPPORTED;  // whole 128-byte K atoms and 64-column output chunks
-    // fp8: one 128-wide scale block per K step and 256-column tiles (two weight-scale
-    // blocks each)
-    if (fp8 && (cfg->K % 128 != 0 || cfg->N % 256 != 0))
+    // fp8: one 128-wide scale block per K step, whole 128-column weight-scale blocks
+    if (fp8 && (cfg->K % 128 != 0 || cfg->N % 128 != 0))
         return EP_ERR_UNSUPPORTED;
     if (fp8 && (!a->a_scales || !a->w_scales ||
                 (reinterpret_cast<uintptr_t>(a->a_scales) & 3u) ||
@@ -193,7 +199,8 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     if (num_sms <= 0)
         return EP_ERR_CUDA;
 
-    const int bn = fp8 ? 256 : (cfg->N % 256 == 0 ? 256 : (cfg->N % 128 == 0 ? 128 : 64));
+    const int bn = fp8 ? fp8_tile_n(cfg->N)
+                       : (cfg->N % 256 == 0 ? 256 : (cfg->N % 128 == 0 ? 128 : 64));
     const int El = cfg->n_local_experts;
     const int elem = fp8 ? 1 : 2;
     const int box_k = 128 / elem;  // one 128-byte swizzle atom of K per stage
@@ -245,7 +252,7 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     const int grid = static_cast<int>(max_tiles < num_sms ? (max_tiles < 1 ? 1 : max_tiles)
                                                           : num_sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return cuda_status(fp8 ? ep::launch_gemm_send_fp8(ta, tb, p, grid, s)
+    return cuda_status(fp8 ? ep::launch_gemm_send_fp8(ta, tb, p, bn, grid, s)
                            : ep::launch_gemm_send_bf16(ta, tb, p, bn, grid, s));
 }
 

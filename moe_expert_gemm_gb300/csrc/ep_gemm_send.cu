@@ -231,6 +231,8 @@ __global__ void __launch_bounds__(224, 1)
                 tmem_ld_32x32b_x32(t_row + sub * 64, v0);
                 tmem_ld_32x32b_x32(t_row + sub * 64 + 32, v1);
                 tmem_ld_wait();
+                tmem_regs_ready(v0);
+                tmem_regs_ready(v1);
                 // fp32 -> bf16 (nearest even), this thread's row, 8 chunks of 16 bytes
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {

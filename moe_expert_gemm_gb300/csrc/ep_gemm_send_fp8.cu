@@ -9,17 +9,19 @@
 // on the tensor cores, and warps outside the MMA path scale and accumulate the
 // partials ("promotion") in registers.
 //
-// Design for sm_103a, one persistent CTA per SM, 352 threads:
-//  warp 0     TMA: A box 128 (K bytes) x 128 rows, W box 128 x 256, 128-byte swizzle,
-//             4-stage ring; one stage is exactly one scale block.
-//  warp 1     TMEM (512 columns = two 128 x 256 fp32 partial buffers) and the MMA:
-//             tcgen05.mma kind::f8f6f4, e4m3 x e4m3, M 128, N 256, K 32 per
-//             instruction; one partial per K block, alternating buffers.
+// Design for sm_103a, one persistent CTA per SM, 352 threads, column tile BN = 256
+// (128 where N is not a multiple of 256):
+//  warp 0     TMA: A box 128 (K bytes) x 128 rows, W box 128 x BN, 128-byte swizzle;
+//             one stage is exactly one scale block (4 stages; 6 for BN 128).
+//  warp 1     TMEM (512 columns = 512/BN fp32 partial buffers of 128 x BN) and the MMA:
+//             tcgen05.mma kind::f8f6f4, e4m3 x e4m3, M 128, N BN, K 32 per instruction;
+//             one partial per K block, buffers in rotation.
 //  warp 2     completion counting + signalling (shared with the bf16 kernel).
 //  warps 3-10 promotion + epilogue: warp w reads TMEM lane quarter w % 4 and column
-//             half (w - 3) / 4; each thread keeps its row's 128 fp32 accumulators,
-//             adds sa[m, kb] * sw[e, n/128, kb] * partial per K block, then rounds to
-//             bf16 and sends the row in 64-byte pieces (4 lanes per row).
+//             half (w - 3) / 4; each thread keeps its row's BN/2 fp32 accumulators
+//             (as pairs, updated with paired FMAs), adds sa[m, kb] * sw[e, n/128, kb] *
+//             partial per K block, then rounds to bf16 and sends the row in 64-byte
+//             pieces (4 lanes per row).
 #include <cuda_bf16.h>
 
 #include "ep_internal.h"
@@ -40,9 +42,12 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
         : "memory");
 }
 
+template <int BN_>
 struct Fp8Layout {
-    static constexpr int BN = 256;
-    static constexpr int STAGES = 4;
+    static constexpr int BN = BN_;
+    static constexpr int STAGES = BN == 128 ? 6 : 4;
+    static constexpr int kBufs = 512 / BN;  // fp32 partial buffers that fit in TMEM
+    static constexpr int kHalfCols = BN / 2;  // columns per promotion warp
     static constexpr int kABytes = BM * kRowBytesK;  // 128 rows x 128 e4m3
     static constexpr int kBBytes = BN * kRowBytesK;  // 256 rows x 128 e4m3
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -53,7 +58,7 @@ struct Fp8Layout {
     static constexpr int kOffB = kOffA + STAGES * kABytes;
     static constexpr int kOffStaging = kOffB + STAGES * kBBytes;
     static constexpr int kOffBars = kOffStaging + kPromoWarps * kWarpStaging;
-    static constexpr int kNumBars = 2 * STAGES + 5;  // full, empty, pfull x2, pfree x2, mma_done
+    static constexpr int kNumBars = 2 * STAGES + 2 * kBufs + 1;  // full, empty, pfull, pfree, done
     static constexpr int kOffSink = (kOffBars + kNumBars * 8 + 15) / 16 * 16;
     static constexpr int kEnd = kOffSink + static_cast<int>(sizeof(SinkShared));
     static constexpr int kSmemBytes = kEnd + 1024;
@@ -62,14 +67,17 @@ struct Fp8Layout {
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
+template <int BN_>
 __global__ void __launch_bounds__(352, 1)
     gemm_send_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b,
                          const __grid_constant__ SendParams p)
 {
-    using L = Fp8Layout;
+    using L = Fp8Layout<BN_>;
     constexpr int BN = L::BN;
     constexpr int STAGES = L::STAGES;
+    constexpr int NBUF = L::kBufs;
+    constexpr int HC = L::kHalfCols;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -79,8 +87,8 @@ __global__ void __launch_bounds__(352, 1)
     uint64_t *full = bars;
     uint64_t *empty = bars + STAGES;
     uint64_t *pfull = bars + 2 * STAGES;
-    uint64_t *pfree = pfull + 2;
-    uint64_t *mma_done = pfree + 2;
+    uint64_t *pfree = pfull + NBUF;
+    uint64_t *mma_done = pfree + NBUF;
     SinkShared *sh = reinterpret_cast<SinkShared *>(smem + L::kOffSink);
     volatile int *abort_flag = &sh->abort_flag;
     const int El = p.El;
@@ -91,7 +99,7 @@ __global__ void __launch_bounds__(352, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NBUF; ++b) {
             mbar_init(&pfull[b], 1);
             mbar_init(&pfree[b], L::kPromoWarps);
         }
@@ -160,7 +168,7 @@ __global__ void __launch_bounds__(352, 1)
             bool ok = true;
             for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
                 for (int kb = 0; kb < nkb; ++kb, ++g) {
-                    const uint32_t pb = g & 1u, pph = (g >> 1) & 1u;
+                    const uint32_t pb = g % NBUF, pph = (g / NBUF) & 1u;
                     if (!mbar_wait(&pfree[pb], pph ^ 1u, p.timeout_ns, abort_flag) ||
                         !mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag)) {
                         ok = false;
@@ -219,38 +227,49 @@ __global__ void __launch_bounds__(352, 1)
             const float *sa = p.a_scales + static_cast<int64_t>(m_s) * nkb;
             const float *sw = p.w_scales +
                               (static_cast<int64_t>(c.e) * n_scale_blocks +
-                               (c.nb * BN + half * 128) / 128) * nkb;
-            float acc[128];
+                               (c.nb * BN + half * HC) / 128) * nkb;
+            // HC fp32 accumulators of this thread's row, as pairs
+            uint64_t acc[HC / 2];
 #pragma unroll
-            for (int j = 0; j < 128; ++j)
-                acc[j] = 0.f;
+            for (int j = 0; j < HC / 2; ++j)
+                acc[j] = 0ull;
             float sa_next = __ldg(sa), sw_next = __ldg(sw);
             bool ok_t = push_ok;
             for (int kb = 0; kb < nkb && ok_t; ++kb, ++g) {
                 const float s = sa_next * sw_next;
+                const uint64_t s2 = pack_f32x2(__float_as_uint(s), __float_as_uint(s));
                 if (kb + 1 < nkb) {
                     sa_next = __ldg(sa + kb + 1);
                     sw_next = __ldg(sw + kb + 1);
                 }
-                const uint32_t pb = g & 1u, pph = (g >> 1) & 1u;
+                const uint32_t pb = g % NBUF, pph = (g / NBUF) & 1u;
                 ok_t = mbar_wait(&pfull[pb], pph, p.timeout_ns, abort_flag);
                 ok_t = __all_sync(0xffffffffu, ok_t);
                 if (!ok_t)
                     break;
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                       pb * BN + half * 128;
+                                       pb * BN + half * HC;
+                // HC/16 groups of 16 columns; the load of group j+1 is in flight while
+                // group j is scaled and added
+                constexpr int NG = HC / 16;
+                uint32_t buf0[16], buf1[16];
+                tmem_ld_32x32b_x16(taddr, buf0);
+                tmem_ld_wait();
+                tmem_regs_ready(buf0);
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    uint32_t v0[16], v1[16];
-                    tmem_ld_32x32b_x16(taddr + c4 * 32, v0);
-                    tmem_ld_32x32b_x16(taddr + c4 * 32 + 16, v1);
-                    tmem_ld_wait();
+                for (int j = 0; j < NG; ++j) {
+                    uint32_t(&cur)[16] = (j & 1) ? buf1 : buf0;
+                    uint32_t(&nxt)[16] = (j & 1) ? buf0 : buf1;
+                    if (j + 1 < NG)
+                        tmem_ld_32x32b_x16(taddr + (j + 1) * 16, nxt);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        acc[c4 * 32 + j] = fmaf(s, __uint_as_float(v0[j]), acc[c4 * 32 + j]);
-                        acc[c4 * 32 + 16 + j] =
-                            fmaf(s, __uint_as_float(v1[j]), acc[c4 * 32 + 16 + j]);
+                    for (int h = 0; h < 8; ++h)
+                        acc[j * 8 + h] = fma_f32x2(pack_f32x2(cur[2 * h], cur[2 * h + 1]), s2,
+                                                   acc[j * 8 + h]);
+                    if (j + 1 < NG) {
+                        tmem_ld_wait();
+                        tmem_regs_ready(nxt);
                     }
                 }
                 // partial read: hand the buffer back to the MMA warp
@@ -270,22 +289,23 @@ __global__ void __launch_bounds__(352, 1)
 
             // bf16 rows, 32 columns at a time: stage, then 4 lanes per row send 64 bytes
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
+            for (int c4 = 0; c4 < HC / 32; ++c4) {
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                     uint32_t w[4];
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
+                        const uint64_t a2 = acc[c4 * 16 + ch * 4 + h];
                         __nv_bfloat162 b = __float22bfloat162_rn(
-                            make_float2(acc[c4 * 32 + ch * 8 + 2 * h],
-                                        acc[c4 * 32 + ch * 8 + 2 * h + 1]));
+                            make_float2(__uint_as_float(static_cast<uint32_t>(a2)),
+                                        __uint_as_float(static_cast<uint32_t>(a2 >> 32))));
                         w[h] = *reinterpret_cast<uint32_t *>(&b);
                     }
                     st_shared_v4(stg + lane * L::kStgRow + ch * 16,
                                  make_uint4(w[0], w[1], w[2], w[3]));
                 }
                 __syncwarp();
-                const int col_byte = (c.nb * BN + half * 128 + c4 * 32) * 2;
+                const int col_byte = (c.nb * BN + half * HC + c4 * 32) * 2;
 #pragma unroll
                 for (int it = 0; it < 4; ++it) {
                     const int r = it * 8 + (lane >> 2);
@@ -330,17 +350,31 @@ __global__ void __launch_bounds__(352, 1)
     }
 }
 
-cudaError_t launch_gemm_send_fp8(const CUtensorMap &ta, const CUtensorMap &tb,
+template <int BN>
+static cudaError_t launch_fp8_bn(const CUtensorMap &ta, const CUtensorMap &tb,
                                  const SendParams &p, int grid, cudaStream_t s)
 {
-    using L = Fp8Layout;
-    cudaError_t err = cudaFuncSetAttribute(gemm_send_fp8_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           L::kSmemBytes);
+    using L = Fp8Layout<BN>;
+    auto kern = gemm_send_fp8_kernel<BN>;
+    cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (err != cudaSuccess)
         return err;
-    gemm_send_fp8_kernel<<<grid, L::kThreads, L::kSmemBytes, s>>>(ta, tb, p);
+    kern<<<grid, L::kThreads, L::kSmemBytes, s>>>(ta, tb, p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_send_fp8(const CUtensorMap &ta, const CUtensorMap &tb,
+                                 const SendParams &p, int bn, int grid, cudaStream_t s)
+{
+    switch (bn) {
+    case 256:
+        return launch_fp8_bn<256>(ta, tb, p, grid, s);
+    case 128:
+        return launch_fp8_bn<128>(ta, tb, p, grid, s);
+    default:
+        return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace ep

@@ -210,6 +210,32 @@ __device__ __forceinline__ void tmem_ld_wait()
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Registers filled by tcgen05.ld hold their values only after tcgen05.wait::ld.
+// Passing them through an (empty) volatile asm placed after the wait makes every
+// later use depend on it, so the compiler cannot hoist a use above the wait.
+template <int N>
+__device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[N])
+{
+#pragma unroll
+    for (int i = 0; i < N; i += 8)
+        asm volatile(""
+                     : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]),
+                       "+r"(r[i + 4]), "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7]));
+}
+
+// Two independent fp32 fused multiply-adds, each rounded to nearest even.
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t pack_f32x2(uint32_t lo, uint32_t hi)
+{
+    return static_cast<uint64_t>(lo) | (static_cast<uint64_t>(hi) << 32);
+}
+
 // Shared-memory matrix descriptor of a K-major operand tile stored as rows of
 // 128 bytes with the 128-byte swizzle (the layout a TMA load with
 // CU_TENSOR_MAP_SWIZZLE_128B writes): 8-row groups 1024 bytes apart. The tile

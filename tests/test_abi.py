@@ -93,9 +93,9 @@ def test_unaligned_operand_rejected(lib):
 
 
 def test_fp8_shape_rules(lib):
-    """Blockwise fp8 needs whole 128-wide scale blocks along K and 256-column tiles."""
+    """Blockwise fp8 needs whole 128-wide scale blocks along K and N."""
     a = ep.ep_send_args()
-    for kw in (dict(K=192), dict(N=384, msg_bytes=768)):
+    for kw in (dict(K=192), dict(N=320, msg_bytes=640)):
         cfg = _cfg(dtype=ep.EP_FP8_1D2D, **kw)
         assert lib.grouped_gemm_combine_send(ctypes.byref(cfg), ctypes.byref(a), None) == \
             ep.EP_ERR_UNSUPPORTED
