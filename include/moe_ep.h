@@ -55,6 +55,7 @@ typedef struct CUstream_st *ep_stream_t;
 #define EP_STATUS_TIMEOUT 0x2u  /* a bounded wait ran out (pipeline barrier or rank flag) */
 #define EP_STATUS_CAPACITY 0x4u /* ep_plan: routed rows exceed max_rows; the plan is empty */
 #define EP_STATUS_ROUTING 0x8u  /* ep_plan: an expert id outside [0, n_ranks*n_local_experts) */
+#define EP_STATUS_INTERNAL 0x10u /* a CTA pair found inconsistent tensor-memory bases: no work done */
 
 /* operand types */
 #define EP_BF16 0     /* bf16 A and W, fp32 accumulation, bf16 rows */

@@ -26,6 +26,7 @@ EP_STATUS_BOUNDS = 0x1
 EP_STATUS_TIMEOUT = 0x2
 EP_STATUS_CAPACITY = 0x4
 EP_STATUS_ROUTING = 0x8
+EP_STATUS_INTERNAL = 0x10
 
 EP_BF16 = 0
 EP_FP8_1D2D = 1

@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libmoe_ep.so")
 
-SOURCES = ["ep_api.cu", "ep_plan.cu", "ep_gemm_send.cu", "ep_gemm_send_fp8.cu", "ep_combine.cu",
+SOURCES = ["ep_api.cu", "ep_plan.cu", "ep_gemm_send.cu", "ep_gemm_send_fp8.cu",
+           "ep_gemm_send_pair.cu", "ep_combine.cu",
            "ep_noalloc.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

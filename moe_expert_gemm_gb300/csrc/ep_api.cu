@@ -206,12 +206,15 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     const int box_k = 128 / elem;  // one 128-byte swizzle atom of K per stage
     const CUtensorMapDataType dt =
         fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    // bf16 with 256-column tiles runs on CTA pairs: each CTA loads half of the W block
+    const bool pair = !fp8 && bn == 256;
     CUtensorMap ta, tb;
     if (!encode_2d(&ta, dt, a->A, cfg->K, a->max_rows, static_cast<uint64_t>(cfg->K) * elem,
                    box_k, ep::BM))
         return EP_ERR_CUDA;
     if (!encode_2d(&tb, dt, a->W, cfg->K, static_cast<uint64_t>(El) * cfg->N,
-                   static_cast<uint64_t>(cfg->K) * elem, box_k, static_cast<uint32_t>(bn)))
+                   static_cast<uint64_t>(cfg->K) * elem, box_k,
+                   static_cast<uint32_t>(pair ? bn / 2 : bn)))
         return EP_ERR_CUDA;
 
     ep::SendParams p;
@@ -252,6 +255,12 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     const int grid = static_cast<int>(max_tiles < num_sms ? (max_tiles < 1 ? 1 : max_tiles)
                                                           : num_sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (pair) {
+        const int64_t pair_tiles = ((a->max_rows + 2 * ep::BM - 1) / (2 * ep::BM) + El) * p.n_blocks;
+        const int max_pairs = static_cast<int>(
+            pair_tiles < num_sms / 2 ? (pair_tiles < 1 ? 1 : pair_tiles) : num_sms / 2);
+        return cuda_status(ep::launch_gemm_send_bf16_pair(ta, tb, p, max_pairs, s));
+    }
     return cuda_status(fp8 ? ep::launch_gemm_send_fp8(ta, tb, p, bn, grid, s)
                            : ep::launch_gemm_send_bf16(ta, tb, p, bn, grid, s));
 }
@@ -311,6 +320,8 @@ const char *ep_strerror(int code)
             return "device status: routed rows exceed the plan capacity";
         if (code & EP_STATUS_ROUTING)
             return "device status: expert id out of range";
+        if (code & EP_STATUS_INTERNAL)
+            return "device status: inconsistent tensor-memory allocation in a CTA pair";
     }
     return "unknown code";
 }

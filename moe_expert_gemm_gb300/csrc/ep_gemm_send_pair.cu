@@ -1,0 +1,356 @@
+// Grouped expert GEMM (bf16) with the fused EP-combine send, on CTA pairs.
+//
+// Same computation and sink as the single-CTA kernel ("EpiloguePeerSink",
+// "P3PeerSendConfig", "ep_signal_completion"); this variant spends half the
+// shared-memory operand traffic per FLOP. Two CTAs of a cluster share one
+// 256 x 256 tile of one expert: CTA r loads its 128 rows of A and the 128-row
+// half r of the W block, and the even CTA issues tcgen05.mma.cta_group::2
+// (M = 256, N = 256, K = 16), which reads the A and B halves from both CTAs'
+// shared memory and writes rows 128 r .. 128 r + 127 of the accumulator into the
+// TMEM of CTA r. Each CTA then drains and sends its own 128 rows exactly as the
+// single-CTA kernel does.
+//
+// Pair protocol:
+//  * both CTAs allocate and later free TMEM together (cta_group::2);
+//  * every stage's TMA loads of both CTAs complete on the even CTA's full barrier,
+//    which expects the bytes of both;
+//  * the even CTA's commits reach both CTAs' stage-free and accumulator-full
+//    barriers (multicast), and both CTAs' epilogues release an accumulator on the
+//    even CTA's barrier;
+//  * a cluster barrier after set-up (all barriers initialised, TMEM allocated) and
+//    one before the TMEM is freed (no MMA still writing the peer's TMEM).
+// All waits except these two cluster barriers are bounded; every role reaches
+// the final cluster barrier on every path.
+#include <cuda_bf16.h>
+
+#include "ep_internal.h"
+#include "ep_ptx.cuh"
+#include "ep_sink.cuh"
+
+namespace ep {
+
+struct PairLayout {
+    static constexpr int BN = 256;
+    static constexpr int STAGES = 6;
+    static constexpr int kAccStages = 1;              // TMEM accumulators per CTA
+    static constexpr int kTileRows = 2 * BM;          // rows of a pair tile
+    static constexpr int kABytes = BM * kRowBytesK;   // this CTA's 128 rows of A
+    static constexpr int kBBytes = (BN / 2) * kRowBytesK;  // this CTA's half of the W block
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kEpiWarps = 4;
+    static constexpr int kWarpStaging = 32 * 128;
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + STAGES * kABytes;
+    static constexpr int kOffStaging = kOffB + STAGES * kBBytes;
+    static constexpr int kOffBars = kOffStaging + kEpiWarps * kWarpStaging;
+    static constexpr int kNumBars = 2 * STAGES + 5;
+    static constexpr int kOffSink = (kOffBars + kNumBars * 8 + 15) / 16 * 16;
+    static constexpr int kEnd = kOffSink + static_cast<int>(sizeof(SinkShared));
+    static constexpr int kSmemBytes = kEnd + 1024;
+    static constexpr uint32_t kTmemCols = kAccStages * BN;
+    static constexpr int kThreads = 224;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
+    gemm_send_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                               const __grid_constant__ CUtensorMap tmap_b,
+                               const __grid_constant__ SendParams p)
+{
+    using L = PairLayout;
+    constexpr int BN = L::BN;
+    constexpr int STAGES = L::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs; 1: its peer
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBars);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES;
+    uint64_t *acc_full = bars + 2 * STAGES;
+    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *mma_done = acc_empty + 2;
+    SinkShared *sh = reinterpret_cast<SinkShared *>(smem + L::kOffSink);
+    volatile int *abort_flag = &sh->abort_flag;
+    const int El = p.El;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < L::kAccStages; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], 2 * L::kEpiWarps);  // both CTAs' epilogue warps
+        }
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+    }
+    sink_prologue(p, sh, L::kTileRows);
+    if (warp == 1) {
+        __syncwarp();
+        tmem_alloc_pair(&sh->tmem_slot, L::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmap_a);
+        tma_prefetch_map(&tmap_b);
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // the peer's barriers exist before anyone signals them
+    tc_fence_after();
+    const uint32_t tmem_base = sh->tmem_slot;
+    // the pair MMA writes both CTAs' TMEM at one address: both allocations must agree
+    const uint32_t peer_base = ld_shared_cluster_u32(mapa_shared(smem_u32(&sh->tmem_slot), rank ^ 1u));
+    const bool tmem_ok = peer_base == tmem_base;
+    if (!tmem_ok && threadIdx.x == 0)
+        atomicOr(p.status, EP_STATUS_INTERNAL);
+    const int total_tiles = tmem_ok ? sh->tile_start[El] : 0;
+
+    if (warp == 0) {
+        // ------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t used_mask = 0, last_parity = 0;
+            bool ok = true;
+            for (int t = pair; t < total_tiles && ok; t += n_pairs) {
+                const TileCoord c =
+                    decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks, L::kTileRows);
+                const int a_row = c.m_abs + static_cast<int>(rank) * BM;
+                const int w_row = c.e * p.N + c.nb * BN + static_cast<int>(rank) * (BN / 2);
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full_lead = mapa_shared(smem_u32(&full[stage]), 0);
+                    if (leader)
+                        mbar_arrive_expect_tx(&full[stage], 2 * L::kStageBytes);
+                    tma_load_2d_pair(smem + L::kOffA + stage * L::kABytes, &tmap_a, full_lead,
+                                     kb * 64, a_row);
+                    tma_load_2d_pair(smem + L::kOffB + stage * L::kBBytes, &tmap_b, full_lead,
+                                     kb * 64, w_row);
+                    used_mask |= 1u << stage;
+                    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok)
+                raise_abort(p.status, abort_flag);
+            volatile int no_abort = 0;
+            if (leader) {
+                // the even CTA's full barriers count both CTAs' loads
+                for (int s = 0; s < STAGES; ++s)
+                    if (used_mask & (1u << s))
+                        mbar_wait_cluster(&full[s], (last_parity >> s) & 1u, p.timeout_ns,
+                                          &no_abort);
+            } else if (!ok) {
+                // give loads already issued time to land before this CTA may exit
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 50000) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ----------------------------------------------------------- MMA issuer
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = make_idesc(1u, 2 * BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int i = 0;
+            for (int t = pair; t < total_tiles && ok; t += n_pairs, ++i) {
+                const int as = i % L::kAccStages;
+                const uint32_t aphase = (i / L::kAccStages) & 1;
+                if (!mbar_wait_cluster(&acc_empty[as], aphase ^ 1u, p.timeout_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as * BN);
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!mbar_wait_cluster(&full[stage], phase, p.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + L::kOffA + stage * L::kABytes);
+                    const uint32_t b_addr = smem_u32(smem + L::kOffB + stage * L::kBBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f16_pair(d_tmem, desc_kmajor_sw128(a_addr + kk * 32),
+                                     desc_kmajor_sw128(b_addr + kk * 32), idesc,
+                                     (kb | kk) != 0 ? 1u : 0u);
+                    mma_commit_pair(&empty[stage], 0x3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                mma_commit_pair(&acc_full[as], 0x3);
+            }
+            if (!ok)
+                raise_abort(p.status, abort_flag);
+            mma_commit_pair(mma_done, 0x1);
+            volatile int no_abort = 0;
+            mbar_wait_cluster(mma_done, 0, p.timeout_ns, &no_abort);
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // --------------------------------------------------- epilogue + sink
+        const int q = warp & 3;
+        const int epi_tid = threadIdx.x - 64;
+        const uint32_t stg = smem_u32(smem + L::kOffStaging + (warp - 2) * L::kWarpStaging);
+        uint64_t *trace = epi_tid == 0 ? trace_block(p) : nullptr;
+        if (trace)
+            trace[1] = globaltimer_ns();
+        uint32_t acc_empty_lead[L::kAccStages];
+#pragma unroll
+        for (int a = 0; a < L::kAccStages; ++a)
+            acc_empty_lead[a] = mapa_shared(smem_u32(&acc_empty[a]), 0);
+
+        bool ok = true;
+        bool push_ok = true;
+        int i = 0;
+        for (int t = pair; t < total_tiles; t += n_pairs, ++i) {
+            const TileCoord c =
+                decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks, L::kTileRows);
+            const int as = i % L::kAccStages;
+            const uint32_t aphase = (i / L::kAccStages) & 1;
+            const int row0 = c.m_abs + static_cast<int>(rank) * BM;
+            uint8_t *row_base = resolve_row(p, sh, c, row0 + q * 32 + lane);
+
+            ok = mbar_wait_cluster(&acc_full[as], aphase, p.timeout_ns, abort_flag) && push_ok;
+            ok = named_bar_and(2, 128, ok);
+            if (!ok)
+                break;
+            tc_fence_after();
+            uint64_t *rec = (trace && i < p.trace_records) ? trace + 2 + 4 * i : nullptr;
+            if (rec) {
+                rec[0] = static_cast<uint64_t>(t) | (static_cast<uint64_t>(c.e) << 32);
+                rec[1] = globaltimer_ns();
+            }
+
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(as * BN);
+#pragma unroll 1
+            for (int sub = 0; sub < BN / 64; ++sub) {
+                uint32_t v0[32], v1[32];
+                tmem_ld_32x32b_x32(t_row + sub * 64, v0);
+                tmem_ld_32x32b_x32(t_row + sub * 64 + 32, v1);
+                tmem_ld_wait();
+                tmem_regs_ready(v0);
+                tmem_regs_ready(v1);
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint32_t *v = ch < 4 ? v0 + ch * 8 : v1 + (ch - 4) * 8;
+                    uint32_t w[4];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        __nv_bfloat162 b = __float22bfloat162_rn(
+                            make_float2(__uint_as_float(v[2 * h]), __uint_as_float(v[2 * h + 1])));
+                        w[h] = *reinterpret_cast<uint32_t *>(&b);
+                    }
+                    st_shared_v4(stg + lane * 128 + ((ch ^ (lane & 7)) << 4),
+                                 make_uint4(w[0], w[1], w[2], w[3]));
+                }
+                __syncwarp();
+                const int col_byte = (c.nb * BN + sub * 64) * 2;
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int row = it * 4 + (lane >> 3);
+                    const int ch = lane & 7;
+                    const unsigned long long base = __shfl_sync(
+                        0xffffffffu, reinterpret_cast<unsigned long long>(row_base), row);
+                    const uint4 val = ld_shared_v4(stg + row * 128 + ((ch ^ (row & 7)) << 4));
+                    if (base != 0ull)
+                        st_global_v4(reinterpret_cast<uint8_t *>(base) + col_byte + ch * 16, val);
+                }
+                __syncwarp();
+            }
+            // this CTA's half of the accumulator is drained: tell the even CTA
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_cluster(acc_empty_lead[as]);
+
+            if (p.sink_enabled) {
+                named_bar_sync(1, 128);
+                if (epi_tid == 0) {
+                    if (rec)
+                        rec[2] = globaltimer_ns();
+                    // each CTA counts its half of every pair tile of the expert
+                    const int tiles_e =
+                        2 * ((c.m_end - sh->eoff[c.e] + L::kTileRows - 1) / L::kTileRows) *
+                        p.n_blocks;
+                    push_ok = push_tile_done(p, sh, c.e, rec ? i : -1, tiles_e);
+                }
+            } else if (rec) {
+                rec[2] = rec[3] = globaltimer_ns();
+            }
+        }
+        if (epi_tid == 0) {
+            if (trace)
+                trace[0] = static_cast<uint64_t>(i);
+            close_queue(sh);
+            if (!push_ok)
+                raise_abort(p.status, abort_flag);
+        }
+        if (!ok && lane == 0)
+            raise_abort(p.status, abort_flag);
+    } else {
+        // ------------------------------------------- completion counting + signalling
+        if (lane == 0 && p.sink_enabled)
+            completion_loop(p, sh);
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // no MMA of the pair is still writing either CTA's TMEM
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, L::kTmemCols);
+    }
+}
+
+cudaError_t launch_gemm_send_bf16_pair(const CUtensorMap &ta, const CUtensorMap &tb,
+                                       const SendParams &p, int max_pairs, cudaStream_t s)
+{
+    using L = PairLayout;
+    cudaError_t err = cudaFuncSetAttribute(gemm_send_bf16_pair_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           L::kSmemBytes);
+    if (err != cudaSuccess)
+        return err;
+    // persistent: as many pairs as can be resident at once (clusters are placed
+    // within a GPC), and never more than there are pair tiles
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * max_pairs, 1, 1);
+    cfg.blockDim = dim3(L::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = L::kSmemBytes;
+    cfg.stream = s;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, gemm_send_bf16_pair_kernel, &cfg) != cudaSuccess ||
+        active < 1) {
+        (void)cudaGetLastError();
+        active = max_pairs;
+    }
+    const int pairs = active < max_pairs ? active : max_pairs;
+    gemm_send_bf16_pair_kernel<<<2 * pairs, L::kThreads, L::kSmemBytes, s>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

@@ -80,9 +80,10 @@ struct TileCoord {
 };
 
 // Tiles are numbered expert by expert; within an expert, row block by row block,
-// column block fastest (concurrent blocks share the A rows and sweep W).
+// column block fastest (concurrent blocks share the A rows and sweep W). A row
+// block has `tile_rows` rows (128, or 256 for a CTA pair).
 __device__ __forceinline__ TileCoord decode_tile(int t, const int *tile_start, const int *eoff,
-                                                 int El, int n_blocks)
+                                                 int El, int n_blocks, int tile_rows = BM)
 {
     // the largest expert whose first tile is <= t owns t (empty experts share starts)
     int lo = 0, hi = El - 1;
@@ -98,7 +99,7 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const int *tile_start, c
     const int local = t - tile_start[lo];
     const int mt = local / n_blocks;
     c.nb = local - mt * n_blocks;
-    c.m_abs = eoff[lo] + mt * BM;
+    c.m_abs = eoff[lo] + mt * tile_rows;
     c.m_end = eoff[lo + 1];
     return c;
 }
@@ -106,7 +107,8 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const int *tile_start, c
 // Called by every thread of the block: destination pointers, expert row ranges
 // (made monotone and clamped to the rows of A so that a malformed plan cannot send
 // reads past the plan arrays) and the tile table. Ends with __syncthreads.
-__device__ __forceinline__ void sink_prologue(const SendParams &p, SinkShared *sh)
+__device__ __forceinline__ void sink_prologue(const SendParams &p, SinkShared *sh,
+                                              int tile_rows = BM)
 {
     const int El = p.El;
     if (threadIdx.x < EP_MAX_RANKS) {
@@ -134,7 +136,7 @@ __device__ __forceinline__ void sink_prologue(const SendParams &p, SinkShared *s
         int acc = 0;
         for (int e = 0; e < El; ++e) {
             sh->tile_start[e] = acc;
-            acc += (sh->eoff[e + 1] - sh->eoff[e] + BM - 1) / BM * p.n_blocks;
+            acc += (sh->eoff[e + 1] - sh->eoff[e] + tile_rows - 1) / tile_rows * p.n_blocks;
         }
         sh->tile_start[El] = acc;
     }

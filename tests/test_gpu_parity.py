@@ -177,3 +177,10 @@ def test_trace_records_every_tile_once():
                for b in tr for r in b["records"])
     done = sorted(r["expert"] for r in recs if r["completed"])
     assert done == [e for e in range(w.n_local_experts) if rows[e] > 0]
+
+
+def test_pair_kernel_small_parity():
+    """256-column bf16 tiles run on CTA pairs (M = 256 across two SMs): ragged
+    experts that end inside either CTA's half of a pair tile, empty experts."""
+    w = Workload("pair_small", 4, 3, 2, 300, 320, 512, "bf16", "zipf", "softmax_sel", 54)
+    _check_full(w)
