@@ -136,21 +136,28 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def source_sha(path: str) -> str:
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def kernel_source_sha() -> str:
+    """Digest of every kernel source file (a measurement taken on other sources
+    does not describe the current kernels)."""
+    csrc = os.path.join(ROOT, "moe_expert_gemm_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
 
 
-def measured_traffic(workload: str, kernel: str, src: str):
+def measured_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of `kernel` from a committed ncu summary, if it was
-    taken on the current source of that kernel."""
+    taken on the current kernel sources."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     rec = d.get(workload, {}).get(kernel)
-    if not rec or rec.get("source_sha") != source_sha(src):
+    if not rec or rec.get("source_sha") != kernel_source_sha():
         return None
     return rec.get("bytes_per_launch")
 
@@ -414,8 +421,7 @@ def main():
     peak_bw = float(peaks["hbm_gbs"])
     t_tensor = flops / (peak_tf * 1e12)
     t_hbm = send_bytes / (peak_bw * 1e9)
-    src = os.path.join(ROOT, "moe_expert_gemm_gb300", "csrc", "ep_gemm_send.cu")
-    traffic = measured_traffic(w.name, "grouped_gemm_combine_send", src)
+    traffic = measured_traffic(w.name, "grouped_gemm_combine_send")
     if t_tensor >= t_hbm:
         roof = {"bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": tflops / peak_tf, "traffic": traffic}

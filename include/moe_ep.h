@@ -174,7 +174,9 @@ int ep_plan(const ep_config *cfg, const int32_t *topk_ids, const ep_plan_out *ou
  *                    {tile | expert << 32 | completed-the-expert << 63,
  *                     time the accumulator was ready, time the tile's rows were all
  *                     stored, time its completion counting (and signalling) ended}.
- *                    Allocate at least (#SMs) * (2 + 4*trace_records) words.
+ *                    Allocate at least (#SMs) * (2 + 4*trace_records) words. Where two
+ *                    thread blocks share a tile (bf16, 256-column tiles: CTA pairs),
+ *                    each records it.
  *   timeout_ns       limit of each bounded wait inside the kernel (0: 2 s).
  *   trace_records    records per thread block in `trace` (>= 1 when trace is set).
  */

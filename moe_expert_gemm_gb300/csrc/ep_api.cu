@@ -206,8 +206,12 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     const int box_k = 128 / elem;  // one 128-byte swizzle atom of K per stage
     const CUtensorMapDataType dt =
         fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    // bf16 with 256-column tiles runs on CTA pairs: each CTA loads half of the W block
-    const bool pair = !fp8 && bn == 256;
+    // bf16 with 256-column tiles runs on CTA pairs (each CTA loads half of the W block)
+    // when an expert's expected rows, T*top_k/E_l, fill a 256-row pair tile; with fewer
+    // rows (decode) the pair's extra padded MMA rows cost more than the traffic saved
+    const int64_t rows_per_expert =
+        static_cast<int64_t>(cfg->num_tokens) * cfg->top_k / cfg->n_local_experts;
+    const bool pair = !fp8 && bn == 256 && rows_per_expert >= 2 * ep::BM;
     CUtensorMap ta, tb;
     if (!encode_2d(&ta, dt, a->A, cfg->K, a->max_rows, static_cast<uint64_t>(cfg->K) * elem,
                    box_k, ep::BM))

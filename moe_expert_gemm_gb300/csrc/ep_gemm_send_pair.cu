@@ -32,7 +32,7 @@ namespace ep {
 struct PairLayout {
     static constexpr int BN = 256;
     static constexpr int STAGES = 6;
-    static constexpr int kAccStages = 1;              // TMEM accumulators per CTA
+    static constexpr int kAccStages = 2;              // TMEM accumulators per CTA
     static constexpr int kTileRows = 2 * BM;          // rows of a pair tile
     static constexpr int kABytes = BM * kRowBytesK;   // this CTA's 128 rows of A
     static constexpr int kBBytes = (BN / 2) * kRowBytesK;  // this CTA's half of the W block

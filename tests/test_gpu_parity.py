@@ -114,10 +114,11 @@ def test_edge_parity(name, w, kind):
     _check_full(w, routing)
 
 
-def test_identity_weights_bit_exact():
+@pytest.mark.parametrize("T", [200, 1100])  # single CTAs / CTA pairs (T*top_k/E_l >= 256)
+def test_identity_weights_bit_exact(T):
     """W_e = 2^c I, top_k = 1, gate 1: the whole path moves the activation rows,
     scaled by a power of two, bit for bit."""
-    w = Workload("ident_gpu", 4, 2, 1, 200, 256, 256, "bf16", "uniform", "softmax_indep", 49)
+    w = Workload("ident_gpu", 4, 2, 1, T, 256, 256, "bf16", "uniform", "softmax_indep", 49)
     routing, values = make_inputs(w)
     routing.gates[:] = 1.0
     for q in range(w.n_ranks):
@@ -157,10 +158,13 @@ def test_local_store_when_sink_disabled():
     assert max_rel_err(got, Y) <= TOL["bf16"]
 
 
-def test_trace_records_every_tile_once():
-    """Optional per-tile timestamps: every tile appears once, times are ordered,
-    and exactly the non-empty experts are marked as completed once each."""
-    w = Workload("trace_small", 4, 4, 2, 300, 256, 512, "bf16", "zipf", "softmax_sel", 50)
+@pytest.mark.parametrize("N,T,pair", [(384, 300, False), (512, 600, True)])
+def test_trace_records_every_tile_once(N, T, pair):
+    """Optional per-tile timestamps: every tile appears once per CTA that works on
+    it (single CTAs: once; 256-column bf16 tiles on CTA pairs: once per CTA of the
+    pair), times are ordered, and exactly the non-empty experts are marked as
+    completed, once each."""
+    w = Workload("trace_small", 4, 4, 2, T, 256, N, "bf16", "zipf", "softmax_sel", 50)
     routing, values = make_inputs(w)
     s = build_system(w, routing, values)
     for r in range(w.n_ranks):
@@ -171,8 +175,9 @@ def test_trace_records_every_tile_once():
     assert sum(b["tiles"] for b in tr) == len(recs)
     pl = oracle.plan(w.n_ranks, w.n_local_experts, w.top_k, routing.topk_ids, 1)
     rows = np.diff(pl.expert_offsets)
-    n_blocks = w.N // 256
-    assert sorted(r["tile"] for r in recs) == list(range(int((-(-rows // 128)).sum()) * n_blocks))
+    tile_rows, n_blocks, copies = (256, N // 256, 2) if pair else (128, N // 128, 1)
+    n_tiles = int((-(-rows // tile_rows)).sum()) * n_blocks
+    assert sorted(r["tile"] for r in recs) == sorted(list(range(n_tiles)) * copies)
     assert all(b["t_start"] <= r["t_ready"] <= r["t_stored"] <= r["t_done"]
                for b in tr for r in b["records"])
     done = sorted(r["expert"] for r in recs if r["completed"])
@@ -180,7 +185,8 @@ def test_trace_records_every_tile_once():
 
 
 def test_pair_kernel_small_parity():
-    """256-column bf16 tiles run on CTA pairs (M = 256 across two SMs): ragged
-    experts that end inside either CTA's half of a pair tile, empty experts."""
-    w = Workload("pair_small", 4, 3, 2, 300, 320, 512, "bf16", "zipf", "softmax_sel", 54)
+    """256-column bf16 tiles run on CTA pairs (M = 256 across two SMs) once an
+    expert's expected rows fill a pair tile: ragged experts that end inside
+    either CTA's half of a pair tile, empty experts."""
+    w = Workload("pair_small", 4, 3, 2, 400, 320, 512, "bf16", "zipf", "softmax_sel", 54)
     _check_full(w)
