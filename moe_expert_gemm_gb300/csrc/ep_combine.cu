@@ -8,10 +8,13 @@
 // (src_idx*top_k + src_topk)*msg_bytes + byte_off.
 //
 // HBM-bound: every received byte is read once and every output byte written
-// once. R threads per block acquire the R source flags (bounded waits), then each
-// warp handles 256 contiguous columns of one token: 32 lanes x 16-byte loads of
+// once. R threads per block acquire the R source flags (bounded waits), then a warp
+// handles units of 256 contiguous columns of one token: 32 lanes x 16-byte loads of
 // each of the token's top_k rows, fp32 accumulation in slot order, one 16-byte
-// streaming store. The grid is one wave of 8 blocks per SM with a grid-stride loop.
+// streaming store. A warp takes max(1, 8 / top_k) consecutive units at a time and
+// issues all their loads before accumulating, so each thread keeps about eight
+// 16-byte loads in flight. The grid is at most one wave of 8 blocks per SM with a
+// grid-stride loop.
 #include <cuda_bf16.h>
 
 #include "ep_internal.h"
@@ -20,6 +23,20 @@
 namespace ep {
 
 constexpr int kCombineThreads = 256;
+constexpr int kLoads = 8;  // 16-byte row loads a thread keeps in flight
+
+__device__ __forceinline__ void store_out(const CombineParams &p, int64_t t, int64_t v,
+                                          const float (&acc)[8])
+{
+    uint32_t o[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        __nv_bfloat162 b = __float22bfloat162_rn(make_float2(acc[2 * h], acc[2 * h + 1]));
+        o[h] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    __stcs(reinterpret_cast<uint4 *>(p.out + (t * p.N + v * 8) * 2),
+           make_uint4(o[0], o[1], o[2], o[3]));
+}
 
 __device__ __forceinline__ void accumulate_row(float (&acc)[8], float g, uint4 raw)
 {
@@ -31,14 +48,15 @@ __device__ __forceinline__ void accumulate_row(float (&acc)[8], float g, uint4 r
     }
 }
 
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p)
+// Acquire every source rank's flag (one thread per rank, bounded wait); false when
+// a wait ran out (EP_STATUS_TIMEOUT raised, the block must not read the rows).
+__device__ __forceinline__ bool acquire_source_flags(const CombineParams &p)
 {
     __shared__ int s_ok;
     if (threadIdx.x == 0)
         s_ok = 1;
     __syncthreads();
     if (threadIdx.x < p.n_ranks) {
-        // one thread per source rank acquires that rank's flag (bounded wait)
         const uint64_t *flag = p.recv_count + static_cast<int64_t>(p.El) * p.n_ranks + threadIdx.x;
         const uint64_t t0 = globaltimer_ns();
         while (ld_acquire_sys_u64(flag) != p.epoch) {
@@ -51,13 +69,65 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
         }
     }
     __syncthreads();
-    if (!s_ok)
-        return;
+    return s_ok != 0;
+}
 
+// top_k known at compile time: a warp takes U = max(1, kLoads / K) consecutive units
+// and issues all U*K loads before accumulating any of them.
+template <int K>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p)
+{
+    if (!acquire_source_flags(p))
+        return;
+    constexpr int U = K >= kLoads ? 1 : kLoads / K;
+    const int lane = threadIdx.x & 31;
+    const int warps = kCombineThreads / 32;
+    const int64_t vec_per_row = p.N / 8;  // 16-byte vectors of one output row
+    const int64_t units_per_row = (vec_per_row + 31) / 32;
+    const int64_t units = static_cast<int64_t>(p.T) * units_per_row;
+    for (int64_t u0 = (static_cast<int64_t>(blockIdx.x) * warps + (threadIdx.x >> 5)) * U;
+         u0 < units; u0 += static_cast<int64_t>(gridDim.x) * warps * U) {
+        uint4 r[U][K];
+        int64_t tt[U], vv[U];
+        bool live[U];
+#pragma unroll
+        for (int uu = 0; uu < U; ++uu) {
+            const int64_t u = u0 + uu;
+            tt[uu] = u / units_per_row;
+            vv[uu] = (u - tt[uu] * units_per_row) * 32 + lane;
+            live[uu] = u < units && vv[uu] < vec_per_row;
+#pragma unroll
+            for (int j = 0; j < K; ++j)
+                if (live[uu])
+                    r[uu][j] = __ldcs(reinterpret_cast<const uint4 *>(
+                        p.recv_buf + (tt[uu] * K + j) * p.msg_bytes + vv[uu] * 16));
+        }
+#pragma unroll
+        for (int uu = 0; uu < U; ++uu) {
+            if (!live[uu])
+                continue;
+            float acc[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                acc[c] = 0.f;
+            const float *g = p.gates + tt[uu] * K;
+#pragma unroll
+            for (int j = 0; j < K; ++j)
+                accumulate_row(acc, __ldg(g + j), r[uu][j]);
+            store_out(p, tt[uu], vv[uu], acc);
+        }
+    }
+}
+
+// any other top_k: one unit at a time, its rows streamed kLoads at a time
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel_any(const CombineParams p)
+{
+    if (!acquire_source_flags(p))
+        return;
     const int lane = threadIdx.x & 31;
     const int warps = kCombineThreads / 32;
     const int k = p.top_k;
-    const int64_t vec_per_row = p.N / 8;  // 16-byte vectors of one output row
+    const int64_t vec_per_row = p.N / 8;
     const int64_t units_per_row = (vec_per_row + 31) / 32;
     const int64_t units = static_cast<int64_t>(p.T) * units_per_row;
     for (int64_t u = static_cast<int64_t>(blockIdx.x) * warps + (threadIdx.x >> 5); u < units;
@@ -72,41 +142,64 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
             acc[c] = 0.f;
         const uint8_t *rows = p.recv_buf + t * k * p.msg_bytes + v * 16;
         const float *g = p.gates + t * k;
-        int j = 0;
-        for (; j + 4 <= k; j += 4) {
-            uint4 r[4];
+        for (int j = 0; j < k; j += kLoads) {
+            uint4 r[kLoads];
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj)
-                r[jj] = __ldcs(reinterpret_cast<const uint4 *>(rows + (j + jj) * p.msg_bytes));
+            for (int jj = 0; jj < kLoads; ++jj)
+                if (j + jj < k)
+                    r[jj] = __ldcs(reinterpret_cast<const uint4 *>(rows + (j + jj) * p.msg_bytes));
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj)
-                accumulate_row(acc, __ldg(g + j + jj), r[jj]);
+            for (int jj = 0; jj < kLoads; ++jj)
+                if (j + jj < k)
+                    accumulate_row(acc, __ldg(g + j + jj), r[jj]);
         }
-        for (; j < k; ++j)
-            accumulate_row(acc, __ldg(g + j),
-                           __ldcs(reinterpret_cast<const uint4 *>(rows + j * p.msg_bytes)));
-        uint32_t o[4];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            __nv_bfloat162 b = __float22bfloat162_rn(make_float2(acc[2 * h], acc[2 * h + 1]));
-            o[h] = *reinterpret_cast<uint32_t *>(&b);
-        }
-        __stcs(reinterpret_cast<uint4 *>(p.out + (t * p.N + v * 8) * 2),
-               make_uint4(o[0], o[1], o[2], o[3]));
+        store_out(p, t, v, acc);
     }
+}
+
+template <typename Kern>
+static int blocks_for(Kern kern, int num_sms, int64_t work_blocks)
+{
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCombineThreads, 0) !=
+            cudaSuccess ||
+        per_sm < 1) {
+        (void)cudaGetLastError();
+        per_sm = 1;
+    }
+    const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;  // one resident wave
+    int64_t b = work_blocks < cap ? work_blocks : cap;
+    return static_cast<int>(b < 1 ? 1 : b);
+}
+
+template <int K>
+static cudaError_t launch_k(const CombineParams &p, int num_sms, cudaStream_t s)
+{
+    constexpr int U = K >= kLoads ? 1 : kLoads / K;
+    const int64_t units = static_cast<int64_t>(p.T) * ((p.N / 8 + 31) / 32);
+    const int b = blocks_for(combine_kernel<K>, num_sms, (units + 8 * U - 1) / (8 * U));
+    combine_kernel<K><<<b, kCombineThreads, 0, s>>>(p);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const CombineParams &p, int num_sms, cudaStream_t s)
 {
-    const int64_t units = static_cast<int64_t>(p.T) * ((p.N / 8 + 31) / 32);
-    int64_t blocks = (units + 7) / 8;
-    const int64_t cap = static_cast<int64_t>(num_sms) * (2048 / kCombineThreads);
-    if (blocks > cap)
-        blocks = cap;
-    if (blocks < 1)
-        blocks = 1;
-    combine_kernel<<<static_cast<int>(blocks), kCombineThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    switch (p.top_k) {
+    case 1:
+        return launch_k<1>(p, num_sms, s);
+    case 2:
+        return launch_k<2>(p, num_sms, s);
+    case 4:
+        return launch_k<4>(p, num_sms, s);
+    case 8:
+        return launch_k<8>(p, num_sms, s);
+    default: {
+        const int64_t units = static_cast<int64_t>(p.T) * ((p.N / 8 + 31) / 32);
+        const int b = blocks_for(combine_kernel_any, num_sms, (units + 7) / 8);
+        combine_kernel_any<<<b, kCombineThreads, 0, s>>>(p);
+        return cudaGetLastError();
+    }
+    }
 }
 
 }  // namespace ep

@@ -88,6 +88,9 @@ EDGE = [
                                "softmax_sel", 47), "empty"),
     ("qwen_shape_small", Workload("qwen_small", 8, 16, 8, 48, 1536, 4096, "bf16", "zipf",
                                   "softmax_sel", 48), "random"),
+    # a top_k with no specialised combine (3)
+    ("topk3", Workload("topk3", 4, 2, 3, 40, 128, 256, "bf16", "uniform", "softmax_sel", 55),
+     "random"),
     # blockwise fp8: several scale blocks along K and N, ragged tails, empty experts
     ("fp8_small", Workload("fp8_small", 4, 4, 2, 100, 384, 512, "fp8_1d2d", "uniform",
                            "sigmoid_sel", 51), "random"),
