@@ -102,6 +102,24 @@ int fp8_tile_n(int N)
     return N % 256 == 0 ? 256 : 128;
 }
 
+// Tile order within an expert that moves fewer bytes from DRAM, with `conc` tiles
+// in flight: column blocks fastest re-reads the expert's W once per group of
+// concurrent row blocks; row blocks fastest re-reads its A once per group of
+// concurrent column blocks.
+bool pick_m_fastest(int64_t rows, int64_t tile_rows, int64_t n_blocks, int64_t K, int64_t N,
+                    int64_t elem, int64_t conc)
+{
+    const int64_t m_blocks = (rows + tile_rows - 1) / tile_rows;
+    if (m_blocks <= 1 || conc < 1)
+        return false;
+    const int64_t a_bytes = rows * K * elem, w_bytes = N * K * elem;
+    const int64_t rows_per_wave = conc / n_blocks > 0 ? conc / n_blocks : 1;
+    const int64_t cols_per_wave = conc / m_blocks > 0 ? conc / m_blocks : 1;
+    const int64_t n_fast = a_bytes + (m_blocks + rows_per_wave - 1) / rows_per_wave * w_bytes;
+    const int64_t m_fast = w_bytes + (n_blocks + cols_per_wave - 1) / cols_per_wave * a_bytes;
+    return m_fast < n_fast;
+}
+
 int cuda_status(cudaError_t e)
 {
     return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
@@ -206,12 +224,12 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     const int box_k = 128 / elem;  // one 128-byte swizzle atom of K per stage
     const CUtensorMapDataType dt =
         fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    // bf16 with 256-column tiles runs on CTA pairs (each CTA loads half of the W block)
-    // when an expert's expected rows, T*top_k/E_l, fill a 256-row pair tile; with fewer
-    // rows (decode) the pair's extra padded MMA rows cost more than the traffic saved
+    // 256-column tiles run on CTA pairs (each CTA loads half of the W block) when an
+    // expert's expected rows, T*top_k/E_l, fill a 256-row pair tile; with fewer rows
+    // (decode) the pair's extra padded MMA rows cost more than the traffic saved
     const int64_t rows_per_expert =
         static_cast<int64_t>(cfg->num_tokens) * cfg->top_k / cfg->n_local_experts;
-    const bool pair = !fp8 && bn == 256 && rows_per_expert >= 2 * ep::BM;
+    const bool pair = bn == 256 && rows_per_expert >= 2 * ep::BM;
     CUtensorMap ta, tb;
     if (!encode_2d(&ta, dt, a->A, cfg->K, a->max_rows, static_cast<uint64_t>(cfg->K) * elem,
                    box_k, ep::BM))
@@ -259,13 +277,16 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     const int grid = static_cast<int>(max_tiles < num_sms ? (max_tiles < 1 ? 1 : max_tiles)
                                                           : num_sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    p.m_fastest = pick_m_fastest(rows_per_expert, pair ? 2 * ep::BM : ep::BM, p.n_blocks, cfg->K,
+                                 cfg->N, elem, pair ? num_sms / 2 : grid) ? 1 : 0;
     if (pair) {
         const int64_t pair_tiles = ((a->max_rows + 2 * ep::BM - 1) / (2 * ep::BM) + El) * p.n_blocks;
         const int max_pairs = static_cast<int>(
             pair_tiles < num_sms / 2 ? (pair_tiles < 1 ? 1 : pair_tiles) : num_sms / 2);
-        return cuda_status(ep::launch_gemm_send_bf16_pair(ta, tb, p, max_pairs, s));
+        return cuda_status(fp8 ? ep::launch_gemm_send_fp8(ta, tb, p, bn, true, max_pairs, s)
+                               : ep::launch_gemm_send_bf16_pair(ta, tb, p, max_pairs, s));
     }
-    return cuda_status(fp8 ? ep::launch_gemm_send_fp8(ta, tb, p, bn, grid, s)
+    return cuda_status(fp8 ? ep::launch_gemm_send_fp8(ta, tb, p, bn, false, grid, s)
                            : ep::launch_gemm_send_bf16(ta, tb, p, bn, grid, s));
 }
 

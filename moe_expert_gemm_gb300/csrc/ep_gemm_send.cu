@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(224, 1)
             uint32_t used_mask = 0, last_parity = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-                const TileCoord c = decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks);
+                const TileCoord c = decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks, BM, p.m_fastest);
                 const int w_row = c.e * p.N + c.nb * BN;
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag)) {
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(224, 1)
         bool push_ok = true;  // epi_tid 0: the last hand-off to the completion warp succeeded
         int i = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++i) {
-            const TileCoord c = decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks);
+            const TileCoord c = decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks, BM, p.m_fastest);
             const int as = i & 1;
             const uint32_t aphase = (i >> 1) & 1;
             // resolve this thread's row destination while the MMA runs

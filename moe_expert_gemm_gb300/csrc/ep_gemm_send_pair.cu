@@ -121,7 +121,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
             bool ok = true;
             for (int t = pair; t < total_tiles && ok; t += n_pairs) {
                 const TileCoord c =
-                    decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks, L::kTileRows);
+                    decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks, L::kTileRows, p.m_fastest);
                 const int a_row = c.m_abs + static_cast<int>(rank) * BM;
                 const int w_row = c.e * p.N + c.nb * BN + static_cast<int>(rank) * (BN / 2);
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
@@ -226,7 +226,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
         int i = 0;
         for (int t = pair; t < total_tiles; t += n_pairs, ++i) {
             const TileCoord c =
-                decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks, L::kTileRows);
+                decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks, L::kTileRows, p.m_fastest);
             const int as = i % L::kAccStages;
             const uint32_t aphase = (i / L::kAccStages) & 1;
             const int row0 = c.m_abs + static_cast<int>(rank) * BM;

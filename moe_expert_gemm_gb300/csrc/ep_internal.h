@@ -17,6 +17,7 @@ constexpr int kRowBytesK = 128;  // bytes of K per stage and row: one 128-byte s
 struct SendParams {
     int n_ranks, my_rank, El, top_k, K, N, max_tokens;
     int n_blocks;      // column blocks per expert (N / BN)
+    int m_fastest;     // tile order within an expert: row blocks fastest (else column blocks)
     int num_k_blocks;  // K / (elements per 128 bytes)
     int64_t msg_bytes;
     int64_t max_rows;
@@ -63,8 +64,10 @@ struct CombineParams {
 cudaError_t launch_plan(const PlanParams &p, cudaStream_t s);
 cudaError_t launch_gemm_send_bf16(const CUtensorMap &ta, const CUtensorMap &tb,
                                   const SendParams &p, int bn, int grid, cudaStream_t s);
+// units: thread blocks (single) or CTA pairs (pair) to launch at most
 cudaError_t launch_gemm_send_fp8(const CUtensorMap &ta, const CUtensorMap &tb,
-                                 const SendParams &p, int bn, int grid, cudaStream_t s);
+                                 const SendParams &p, int bn, bool pair, int units,
+                                 cudaStream_t s);
 cudaError_t launch_gemm_send_bf16_pair(const CUtensorMap &ta, const CUtensorMap &tb,
                                        const SendParams &p, int max_pairs, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, int num_sms, cudaStream_t s);

@@ -372,6 +372,18 @@ __device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, u
         : "memory");
 }
 
+// Pair MMA (M = 256 over the two CTAs), e4m3 x e4m3 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on the mbarrier at this offset in every CTA of `mask` when all
 // tcgen05 operations issued so far by this thread have completed.
 __device__ __forceinline__ void mma_commit_pair(uint64_t *bar, uint16_t mask)

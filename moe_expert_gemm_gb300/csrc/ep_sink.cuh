@@ -79,11 +79,14 @@ struct TileCoord {
     int e, m_abs, m_end, nb;
 };
 
-// Tiles are numbered expert by expert; within an expert, row block by row block,
-// column block fastest (concurrent blocks share the A rows and sweep W). A row
-// block has `tile_rows` rows (128, or 256 for a CTA pair).
+// Tiles are numbered expert by expert. Within an expert either the column block
+// runs fastest (concurrent blocks share A rows and sweep W: best when W is the
+// smaller operand) or the row block does (concurrent blocks share a W block and
+// sweep A: best when A is smaller). A row block has `tile_rows` rows (128, or 256
+// for a CTA pair).
 __device__ __forceinline__ TileCoord decode_tile(int t, const int *tile_start, const int *eoff,
-                                                 int El, int n_blocks, int tile_rows = BM)
+                                                 int El, int n_blocks, int tile_rows = BM,
+                                                 bool m_fastest = false)
 {
     // the largest expert whose first tile is <= t owns t (empty experts share starts)
     int lo = 0, hi = El - 1;
@@ -97,8 +100,15 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const int *tile_start, c
     TileCoord c;
     c.e = lo;
     const int local = t - tile_start[lo];
-    const int mt = local / n_blocks;
-    c.nb = local - mt * n_blocks;
+    int mt;
+    if (m_fastest) {
+        const int m_blocks = (eoff[lo + 1] - eoff[lo] + tile_rows - 1) / tile_rows;
+        c.nb = local / m_blocks;
+        mt = local - c.nb * m_blocks;
+    } else {
+        mt = local / n_blocks;
+        c.nb = local - mt * n_blocks;
+    }
     c.m_abs = eoff[lo] + mt * tile_rows;
     c.m_end = eoff[lo + 1];
     return c;

@@ -12,15 +12,22 @@ import oracle
 from oracle.pipeline import SENTINEL_WORD, sampled_pipeline
 from parity_util import (TOL, assert_plan_equal, build_system, combine_rel_err, make_inputs,
                          max_rel_err)
-from synth import WORKLOADS
+from synth import WORKLOADS, Workload
 
 pytestmark = pytest.mark.gpu
 
 
+MEDIUM = {
+    # many rows per expert and wide W blocks: the kernel walks row blocks fastest
+    "fp8_rows_fastest": Workload("fp8_rows_fastest", 2, 2, 2, 4096, 256, 7168, "fp8_1d2d",
+                                 "uniform", "sigmoid_sel", 60),
+}
+
+
 @pytest.mark.parametrize("name", ["mixtral_prefill", "dsv3_decode", "qwen3_skew",
-                                  "dsv3_prefill_fp8"])
+                                  "dsv3_prefill_fp8", "fp8_rows_fastest"])
 def test_full_size_sampled_parity(name):
-    w = WORKLOADS[name]
+    w = WORKLOADS[name] if name in WORKLOADS else MEDIUM[name]
     R, El, k, T, N = w.n_ranks, w.n_local_experts, w.top_k, w.tokens, w.N
     routing, values = make_inputs(w)
     s = build_system(w, routing, values)

@@ -193,3 +193,10 @@ def test_pair_kernel_small_parity():
     either CTA's half of a pair tile, empty experts."""
     w = Workload("pair_small", 4, 3, 2, 400, 320, 512, "bf16", "zipf", "softmax_sel", 54)
     _check_full(w)
+
+
+def test_fp8_pair_kernel_small_parity():
+    """Blockwise fp8 on CTA pairs (expected rows per expert >= 256): ragged experts
+    ending inside either half of a 256-row pair tile, several scale blocks."""
+    w = Workload("fp8_pair_small", 2, 2, 2, 400, 384, 512, "fp8_1d2d", "zipf", "sigmoid_sel", 56)
+    _check_full(w)
