@@ -224,12 +224,14 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     const int box_k = 128 / elem;  // one 128-byte swizzle atom of K per stage
     const CUtensorMapDataType dt =
         fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    // 256-column tiles run on CTA pairs (each CTA loads half of the W block) when an
-    // expert's expected rows, T*top_k/E_l, fill a 256-row pair tile; with fewer rows
-    // (decode) the pair's extra padded MMA rows cost more than the traffic saved
+    // bf16 256-column tiles run on CTA pairs (each CTA loads half of the W block) when
+    // an expert's expected rows, T*top_k/E_l, fill a 256-row pair tile; with fewer rows
+    // (decode) the pair's extra padded MMA rows cost more than the traffic saved. The
+    // fp8 kernel stays on single CTAs: its per-K-block hand-off of partial buffers
+    // between MMA and promotion would cross the pair every K block.
     const int64_t rows_per_expert =
         static_cast<int64_t>(cfg->num_tokens) * cfg->top_k / cfg->n_local_experts;
-    const bool pair = bn == 256 && rows_per_expert >= 2 * ep::BM;
+    const bool pair = !fp8 && bn == 256 && rows_per_expert >= 2 * ep::BM;
     CUtensorMap ta, tb;
     if (!encode_2d(&ta, dt, a->A, cfg->K, a->max_rows, static_cast<uint64_t>(cfg->K) * elem,
                    box_k, ep::BM))
@@ -283,10 +285,9 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
         const int64_t pair_tiles = ((a->max_rows + 2 * ep::BM - 1) / (2 * ep::BM) + El) * p.n_blocks;
         const int max_pairs = static_cast<int>(
             pair_tiles < num_sms / 2 ? (pair_tiles < 1 ? 1 : pair_tiles) : num_sms / 2);
-        return cuda_status(fp8 ? ep::launch_gemm_send_fp8(ta, tb, p, bn, true, max_pairs, s)
-                               : ep::launch_gemm_send_bf16_pair(ta, tb, p, max_pairs, s));
+        return cuda_status(ep::launch_gemm_send_bf16_pair(ta, tb, p, max_pairs, s));
     }
-    return cuda_status(fp8 ? ep::launch_gemm_send_fp8(ta, tb, p, bn, false, grid, s)
+    return cuda_status(fp8 ? ep::launch_gemm_send_fp8(ta, tb, p, bn, grid, s)
                            : ep::launch_gemm_send_bf16(ta, tb, p, bn, grid, s));
 }
 

@@ -10,11 +10,9 @@
 // partials ("promotion") in registers.
 //
 // Design for sm_103a, one persistent CTA per SM, 352 threads, column tile BN = 256
-// (128 where N is not a multiple of 256). With PAIR, two CTAs of a cluster share a
-// 256 x 256 tile: each loads its 128 rows of A and its 128-row half of the W block,
-// the even CTA issues tcgen05.mma.cta_group::2 (M = 256), each CTA promotes and sends
-// its own 128 rows; the pair protocol is the one of the bf16 pair kernel, with the
-// partial buffers' free barrier living in the even CTA. Without PAIR:
+// (128 where N is not a multiple of 256). The kernel stays on single CTAs: with two
+// partial buffers the MMA -> promotion -> MMA hand-off is on the critical path of
+// every K block, and across a CTA pair that round trip doubles.
 //  warp 0     TMA: A box 128 (K bytes) x 128 rows, W box 128 x BN, 128-byte swizzle;
 //             one stage is exactly one scale block (4 stages; 6 for BN 128).
 //  warp 1     TMEM (512 columns = 512/BN fp32 partial buffers of 128 x BN) and the MMA:
@@ -46,15 +44,14 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
         : "memory");
 }
 
-template <int BN_, bool PAIR>
+template <int BN_>
 struct Fp8Layout {
     static constexpr int BN = BN_;
-    static constexpr int STAGES = PAIR ? 6 : (BN == 128 ? 6 : 4);
+    static constexpr int STAGES = BN == 128 ? 6 : 4;
     static constexpr int kBufs = 512 / BN;    // fp32 partial buffers that fit in TMEM
     static constexpr int kHalfCols = BN / 2;  // columns per promotion warp
-    static constexpr int kTileRows = PAIR ? 2 * BM : BM;
-    static constexpr int kABytes = BM * kRowBytesK;                       // 128 rows x 128 e4m3
-    static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * kRowBytesK;    // this CTA's W rows
+    static constexpr int kABytes = BM * kRowBytesK;  // 128 rows x 128 e4m3
+    static constexpr int kBBytes = BN * kRowBytesK;  // BN rows x 128 e4m3
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kPromoWarps = 8;
     static constexpr int kStgRow = 80;                 // 64 data bytes + 16 pad
@@ -70,42 +67,32 @@ struct Fp8Layout {
     static constexpr uint32_t kTmemCols = 2 * BN;
     static constexpr int kThreads = 32 * (3 + kPromoWarps);
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    static_assert(!PAIR || BN == 256, "pairs use 256-column tiles");
 };
 
-// Bounded wait on a local mbarrier; cluster-scope acquire where the arrivals come
-// from the peer CTA.
-template <bool PAIR>
+// The per-K-block hand-offs (stages, partial buffers) spin on test_wait instead of
+// suspending in try_wait: their round trip is on the critical path of every K block.
 __device__ __forceinline__ bool fp8_wait(uint64_t *bar, uint32_t parity, uint64_t timeout_ns,
                                          volatile int *abort)
 {
-    if constexpr (PAIR)
-        return mbar_wait_cluster(bar, parity, timeout_ns, abort);
-    else
-        return mbar_wait(bar, parity, timeout_ns, abort);
+    return mbar_spin<false>(bar, parity, timeout_ns, abort);
 }
 
-template <int BN_, bool PAIR>
+template <int BN_>
 __global__ void __launch_bounds__(352, 1)
     gemm_send_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b,
                          const __grid_constant__ SendParams p)
 {
-    using L = Fp8Layout<BN_, PAIR>;
+    using L = Fp8Layout<BN_>;
     constexpr int BN = L::BN;
     constexpr int STAGES = L::STAGES;
     constexpr int NBUF = L::kBufs;
     constexpr int HC = L::kHalfCols;
-    constexpr int TR = L::kTileRows;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // 0 issues the MMAs
-    const bool leader = rank == 0;
-    const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    const int n_units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBars);
     uint64_t *full = bars;
     uint64_t *empty = bars + STAGES;
@@ -124,21 +111,16 @@ __global__ void __launch_bounds__(352, 1)
         }
         for (int b = 0; b < NBUF; ++b) {
             mbar_init(&pfull[b], 1);
-            mbar_init(&pfree[b], (PAIR ? 2 : 1) * L::kPromoWarps);  // both CTAs' warps
+            mbar_init(&pfree[b], L::kPromoWarps);
         }
         mbar_init(mma_done, 1);
         fence_mbar_init();
     }
-    sink_prologue(p, sh, TR);
+    sink_prologue(p, sh);
     if (warp == 1) {
         __syncwarp();
-        if constexpr (PAIR) {
-            tmem_alloc_pair(&sh->tmem_slot, L::kTmemCols);
-            tmem_relinquish_pair();
-        } else {
-            tmem_alloc(&sh->tmem_slot, L::kTmemCols);
-            tmem_relinquish();
-        }
+        tmem_alloc(&sh->tmem_slot, L::kTmemCols);
+        tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tmap_a);
@@ -146,19 +128,9 @@ __global__ void __launch_bounds__(352, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if constexpr (PAIR)
-        cluster_sync_all();  // the peer's barriers exist before anyone signals them
     tc_fence_after();
     const uint32_t tmem_base = sh->tmem_slot;
-    bool tmem_ok = true;
-    if constexpr (PAIR) {
-        // the pair MMA writes both CTAs' TMEM at one address: both allocations must agree
-        tmem_ok = ld_shared_cluster_u32(mapa_shared(smem_u32(&sh->tmem_slot), rank ^ 1u)) ==
-                  tmem_base;
-        if (!tmem_ok && threadIdx.x == 0)
-            atomicOr(p.status, EP_STATUS_INTERNAL);
-    }
-    const int total_tiles = tmem_ok ? sh->tile_start[El] : 0;
+    const int total_tiles = sh->tile_start[El];
 
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
@@ -167,29 +139,20 @@ __global__ void __launch_bounds__(352, 1)
             uint32_t phase = 0;
             uint32_t used_mask = 0, last_parity = 0;
             bool ok = true;
-            for (int t = unit; t < total_tiles && ok; t += n_units) {
+            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
                 const TileCoord c =
-                    decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks, TR, p.m_fastest);
-                const int a_row = c.m_abs + static_cast<int>(rank) * BM;
-                const int w_row = c.e * p.N + c.nb * BN + static_cast<int>(rank) * (BN / 2);
+                    decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks, BM, p.m_fastest);
+                const int w_row = c.e * p.N + c.nb * BN;
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!fp8_wait<PAIR>(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag)) {
+                    if (!fp8_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    uint8_t *a_dst = smem + L::kOffA + stage * L::kABytes;
-                    uint8_t *b_dst = smem + L::kOffB + stage * L::kBBytes;
-                    if constexpr (PAIR) {
-                        const uint32_t full_lead = mapa_shared(smem_u32(&full[stage]), 0);
-                        if (leader)
-                            mbar_arrive_expect_tx(&full[stage], 2 * L::kStageBytes);
-                        tma_load_2d_pair(a_dst, &tmap_a, full_lead, kb * 128, a_row);
-                        tma_load_2d_pair(b_dst, &tmap_b, full_lead, kb * 128, w_row);
-                    } else {
-                        mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
-                        tma_load_2d(a_dst, &tmap_a, &full[stage], kb * 128, a_row);
-                        tma_load_2d(b_dst, &tmap_b, &full[stage], kb * 128, w_row);
-                    }
+                    mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
+                    tma_load_2d(smem + L::kOffA + stage * L::kABytes, &tmap_a, &full[stage],
+                                kb * 128, c.m_abs);
+                    tma_load_2d(smem + L::kOffB + stage * L::kBBytes, &tmap_b, &full[stage],
+                                kb * 128, w_row);
                     used_mask |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -200,34 +163,27 @@ __global__ void __launch_bounds__(352, 1)
             }
             if (!ok)
                 raise_abort(p.status, abort_flag);
+            // loads complete whether or not anyone consumes them: wait for the last
+            // one of every stage before the block may exit
             volatile int no_abort = 0;
-            if (leader) {
-                // loads complete whether or not anyone consumes them: wait for the last
-                // one of every stage (in a pair the even CTA's barriers count both CTAs')
-                for (int s = 0; s < STAGES; ++s)
-                    if (used_mask & (1u << s))
-                        fp8_wait<PAIR>(&full[s], (last_parity >> s) & 1u, p.timeout_ns,
-                                       &no_abort);
-            } else if (!ok) {
-                const uint64_t t0 = globaltimer_ns();  // let issued loads land before exit
-                while (globaltimer_ns() - t0 < 50000) {
-                }
-            }
+            for (int s = 0; s < STAGES; ++s)
+                if (used_mask & (1u << s))
+                    fp8_wait(&full[s], (last_parity >> s) & 1u, p.timeout_ns, &no_abort);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMA issuer
-        if (lane == 0 && leader) {
-            constexpr uint32_t idesc = make_idesc(0u, PAIR ? 2 * BM : BM, BN);  // e4m3 -> fp32
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(0u, BM, BN);  // e4m3 x e4m3 -> fp32
             int stage = 0;
             uint32_t phase = 0;
             uint32_t g = 0;  // K blocks issued so far (selects the partial buffer)
             bool ok = true;
-            for (int t = unit; t < total_tiles && ok; t += n_units) {
+            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
                 for (int kb = 0; kb < nkb; ++kb, ++g) {
                     const uint32_t pb = g % NBUF, pph = (g / NBUF) & 1u;
-                    if (!fp8_wait<PAIR>(&pfree[pb], pph ^ 1u, p.timeout_ns, abort_flag) ||
-                        !fp8_wait<PAIR>(&full[stage], phase, p.timeout_ns, abort_flag)) {
+                    if (!fp8_wait(&pfree[pb], pph ^ 1u, p.timeout_ns, abort_flag) ||
+                        !fp8_wait(&full[stage], phase, p.timeout_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -236,22 +192,11 @@ __global__ void __launch_bounds__(352, 1)
                     const uint32_t b_addr = smem_u32(smem + L::kOffB + stage * L::kBBytes);
                     const uint32_t d_tmem = tmem_base + pb * BN;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        if constexpr (PAIR)
-                            mma_f8_pair(d_tmem, desc_kmajor_sw128(a_addr + kk * 32),
-                                        desc_kmajor_sw128(b_addr + kk * 32), idesc,
-                                        kk != 0 ? 1u : 0u);
-                        else
-                            mma_f8(d_tmem, desc_kmajor_sw128(a_addr + kk * 32),
-                                   desc_kmajor_sw128(b_addr + kk * 32), idesc, kk != 0 ? 1u : 0u);
-                    }
-                    if constexpr (PAIR) {
-                        mma_commit_pair(&empty[stage], 0x3);
-                        mma_commit_pair(&pfull[pb], 0x3);
-                    } else {
-                        mma_commit(&empty[stage]);
-                        mma_commit(&pfull[pb]);
-                    }
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f8(d_tmem, desc_kmajor_sw128(a_addr + kk * 32),
+                               desc_kmajor_sw128(b_addr + kk * 32), idesc, kk != 0 ? 1u : 0u);
+                    mma_commit(&empty[stage]);
+                    mma_commit(&pfull[pb]);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -260,17 +205,14 @@ __global__ void __launch_bounds__(352, 1)
             }
             if (!ok)
                 raise_abort(p.status, abort_flag);
-            if constexpr (PAIR)
-                mma_commit_pair(mma_done, 0x1);
-            else
-                mma_commit(mma_done);
+            mma_commit(mma_done);
             volatile int no_abort = 0;
-            fp8_wait<PAIR>(mma_done, 0, p.timeout_ns, &no_abort);
+            fp8_wait(mma_done, 0, p.timeout_ns, &no_abort);
         }
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------- completion counting + signalling
-        if (lane == 0 && p.sink_enabled && tmem_ok)
+        if (lane == 0 && p.sink_enabled)
             completion_loop(p, sh);
         __syncwarp();
     } else {
@@ -284,19 +226,15 @@ __global__ void __launch_bounds__(352, 1)
         uint64_t *trace = ptid == 0 ? trace_block(p) : nullptr;
         if (trace)
             trace[1] = globaltimer_ns();
-        uint32_t pfree_lead[NBUF];
-#pragma unroll
-        for (int b = 0; b < NBUF; ++b)
-            pfree_lead[b] = PAIR ? mapa_shared(smem_u32(&pfree[b]), 0) : 0u;
 
         bool ok = true;
         bool push_ok = true;
         uint32_t g = 0;
         int i = 0;
-        for (int t = unit; t < total_tiles; t += n_units, ++i) {
+        for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++i) {
             const TileCoord c =
-                decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks, TR, p.m_fastest);
-            const int m = c.m_abs + static_cast<int>(rank) * BM + row;
+                decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks, BM, p.m_fastest);
+            const int m = c.m_abs + row;
             uint8_t *row_base = resolve_row(p, sh, c, m);
             // scale rows (rows past the tile's group read the last row's scales: unused)
             const int m_s = m < p.max_rows ? m : static_cast<int>(p.max_rows) - 1;
@@ -319,7 +257,7 @@ __global__ void __launch_bounds__(352, 1)
                     sw_next = __ldg(sw + kb + 1);
                 }
                 const uint32_t pb = g % NBUF, pph = (g / NBUF) & 1u;
-                ok_t = fp8_wait<PAIR>(&pfull[pb], pph, p.timeout_ns, abort_flag);
+                ok_t = fp8_wait(&pfull[pb], pph, p.timeout_ns, abort_flag);
                 ok_t = __all_sync(0xffffffffu, ok_t);
                 if (!ok_t)
                     break;
@@ -351,12 +289,8 @@ __global__ void __launch_bounds__(352, 1)
                 // partial read: hand the buffer back to the MMA warp
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    if constexpr (PAIR)
-                        mbar_arrive_cluster(pfree_lead[pb]);
-                    else
-                        mbar_arrive(&pfree[pb]);
-                }
+                if (lane == 0)
+                    mbar_arrive(&pfree[pb]);
             }
             ok = named_bar_and(2, 256, ok_t);
             if (!ok)
@@ -404,9 +338,7 @@ __global__ void __launch_bounds__(352, 1)
                 if (ptid == 0) {
                     if (rec)
                         rec[2] = globaltimer_ns();
-                    // in a pair each CTA counts its half of every tile of the expert
-                    const int tiles_e = (PAIR ? 2 : 1) * ((c.m_end - sh->eoff[c.e] + TR - 1) / TR) *
-                                        p.n_blocks;
+                    const int tiles_e = (c.m_end - sh->eoff[c.e] + BM - 1) / BM * p.n_blocks;
                     push_ok = push_tile_done(p, sh, c.e, rec ? i : -1, tiles_e);
                 }
             } else if (rec) {
@@ -426,66 +358,34 @@ __global__ void __launch_bounds__(352, 1)
 
     tc_fence_before();
     __syncthreads();
-    if constexpr (PAIR)
-        cluster_sync_all();  // no MMA of the pair is still writing either CTA's TMEM
     if (warp == 1) {
         tc_fence_after();
-        if constexpr (PAIR)
-            tmem_dealloc_pair(tmem_base, L::kTmemCols);
-        else
-            tmem_dealloc(tmem_base, L::kTmemCols);
+        tmem_dealloc(tmem_base, L::kTmemCols);
     }
 }
 
-template <int BN, bool PAIR>
-static cudaError_t launch_fp8(const CUtensorMap &ta, const CUtensorMap &tb, const SendParams &p,
-                              int units, cudaStream_t s)
+template <int BN>
+static cudaError_t launch_fp8_bn(const CUtensorMap &ta, const CUtensorMap &tb,
+                                 const SendParams &p, int grid, cudaStream_t s)
 {
-    using L = Fp8Layout<BN, PAIR>;
-    auto kern = gemm_send_fp8_kernel<BN, PAIR>;
+    using L = Fp8Layout<BN>;
+    auto kern = gemm_send_fp8_kernel<BN>;
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (err != cudaSuccess)
         return err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(L::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = L::kSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    if (PAIR) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        // as many pairs as can be resident at once, never more than asked for
-        cfg.gridDim = dim3(2 * units, 1, 1);
-        int active = 0;
-        if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active < 1) {
-            (void)cudaGetLastError();
-            active = units;
-        }
-        units = active < units ? active : units;
-        cfg.gridDim = dim3(2 * units, 1, 1);
-    } else {
-        cfg.gridDim = dim3(units, 1, 1);
-    }
-    err = cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
-    return err != cudaSuccess ? err : cudaGetLastError();
+    kern<<<grid, L::kThreads, L::kSmemBytes, s>>>(ta, tb, p);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_send_fp8(const CUtensorMap &ta, const CUtensorMap &tb,
-                                 const SendParams &p, int bn, bool pair, int units,
-                                 cudaStream_t s)
+                                 const SendParams &p, int bn, int grid, cudaStream_t s)
 {
-    if (pair)
-        return bn == 256 ? launch_fp8<256, true>(ta, tb, p, units, s) : cudaErrorInvalidValue;
     switch (bn) {
     case 256:
-        return launch_fp8<256, false>(ta, tb, p, units, s);
+        return launch_fp8_bn<256>(ta, tb, p, grid, s);
     case 128:
-        return launch_fp8<128, false>(ta, tb, p, units, s);
+        return launch_fp8_bn<128>(ta, tb, p, grid, s);
     default:
         return cudaErrorInvalidValue;
     }

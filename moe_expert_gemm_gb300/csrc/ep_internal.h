@@ -64,10 +64,8 @@ struct CombineParams {
 cudaError_t launch_plan(const PlanParams &p, cudaStream_t s);
 cudaError_t launch_gemm_send_bf16(const CUtensorMap &ta, const CUtensorMap &tb,
                                   const SendParams &p, int bn, int grid, cudaStream_t s);
-// units: thread blocks (single) or CTA pairs (pair) to launch at most
 cudaError_t launch_gemm_send_fp8(const CUtensorMap &ta, const CUtensorMap &tb,
-                                 const SendParams &p, int bn, bool pair, int units,
-                                 cudaStream_t s);
+                                 const SendParams &p, int bn, int grid, cudaStream_t s);
 cudaError_t launch_gemm_send_bf16_pair(const CUtensorMap &ta, const CUtensorMap &tb,
                                        const SendParams &p, int max_pairs, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, int num_sms, cudaStream_t s);

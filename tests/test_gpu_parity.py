@@ -195,8 +195,8 @@ def test_pair_kernel_small_parity():
     _check_full(w)
 
 
-def test_fp8_pair_kernel_small_parity():
-    """Blockwise fp8 on CTA pairs (expected rows per expert >= 256): ragged experts
-    ending inside either half of a 256-row pair tile, several scale blocks."""
+def test_fp8_many_rows_per_expert_parity():
+    """Blockwise fp8 with several 128-row blocks per expert: ragged experts, several
+    scale blocks along K and N."""
     w = Workload("fp8_pair_small", 2, 2, 2, 400, 384, 512, "fp8_1d2d", "zipf", "sigmoid_sel", 56)
     _check_full(w)
