@@ -65,6 +65,9 @@ def parse_args():
                     help="after timing, run one traced send and write its summary here")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override tokens per rank (profiling a smaller case of a workload)")
+    ap.add_argument("--send-warps", type=int, default=-1, choices=[-1, 0, 4],
+                    help="sink placement: -1 library choice, 0 inside the output warps, "
+                         "4 dedicated send warps (bf16)")
     ap.add_argument("--solo", action="store_true",
                     help="profiling aid: only the timed rank's operands, no peer staging, and "
                          "the step is the fused send alone (no combine, no e2e, no baseline)")
@@ -284,7 +287,8 @@ def main():
     ranks = [q] if args.solo else list(range(w.n_ranks))
     values = {r: make_rank_values(w, r, int(rows[r])) for r in ranks}
 
-    s = EpSystem(w.n_ranks, w.n_local_experts, w.top_k, w.tokens, w.K, w.N, w.dtype)
+    s = EpSystem(w.n_ranks, w.n_local_experts, w.top_k, w.tokens, w.K, w.N, w.dtype,
+                 send_warps=args.send_warps)
     s.set_routing(routing.topk_ids)
     for r in ranks:
         s.plan(r)
@@ -445,6 +449,7 @@ def main():
         "config": {"workload": w.name, "n_ranks": w.n_ranks, "n_local_experts": w.n_local_experts,
                    "top_k": w.top_k, "tokens_per_rank": w.tokens, "K": w.K, "N": w.N,
                    "operands": w.dtype, "my_rank": q, "rows": m_rows,
+                   "send_warps": args.send_warps,
                    "l2": ("flushed with a 512 MB write before every step" if flush is not None
                           else f"per-step inputs {step_bytes / 1e6:.0f} MB > L2"),
                    "parallelism": "replicas: one logical rank per GPU" if world > 1

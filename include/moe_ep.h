@@ -77,7 +77,11 @@ typedef struct CUstream_st *ep_stream_t;
  *   dtype                EP_BF16 or EP_FP8_1D2D
  *   send_warps           warps reserved for the sink above the output warps
  *                        ("EpiloguePeerSink" SendWarps): 0 runs the send inside the
- *                        output warps; -1 lets the library choose.
+ *                        output warps; 4 adds four send warps, one per output warp,
+ *                        that store the rows the output warps stage (bf16 only, on
+ *                        single CTAs; fp8 gives EP_ERR_UNSUPPORTED); -1 lets the
+ *                        library choose (today: inside the output warps). Any other
+ *                        value gives EP_ERR_INVALID_ARG.
  */
 typedef struct {
     int32_t n_ranks;

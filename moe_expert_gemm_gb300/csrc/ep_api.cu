@@ -180,7 +180,8 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     if (!a)
         return EP_ERR_INVALID_ARG;
     const bool fp8 = cfg->dtype == EP_FP8_1D2D;
-    if (cfg->send_warps == 4)
+    // dedicated send warps exist in the single-CTA bf16 kernel
+    if (fp8 && cfg->send_warps == 4)
         return EP_ERR_UNSUPPORTED;
     if (!fp8 && (cfg->K % 64 != 0 || cfg->N % 64 != 0))
         return EP_ERR_UNSUPPORTED;  // whole 128-byte K atoms and 64-column output chunks
@@ -228,10 +229,12 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     // an expert's expected rows, T*top_k/E_l, fill a 256-row pair tile; with fewer rows
     // (decode) the pair's extra padded MMA rows cost more than the traffic saved. The
     // fp8 kernel stays on single CTAs: its per-K-block hand-off of partial buffers
-    // between MMA and promotion would cross the pair every K block.
+    // between MMA and promotion would cross the pair every K block. Dedicated send
+    // warps (send_warps = 4) exist in the single-CTA kernel only.
     const int64_t rows_per_expert =
         static_cast<int64_t>(cfg->num_tokens) * cfg->top_k / cfg->n_local_experts;
-    const bool pair = !fp8 && bn == 256 && rows_per_expert >= 2 * ep::BM;
+    const bool pair =
+        !fp8 && bn == 256 && rows_per_expert >= 2 * ep::BM && cfg->send_warps != 4;
     CUtensorMap ta, tb;
     if (!encode_2d(&ta, dt, a->A, cfg->K, a->max_rows, static_cast<uint64_t>(cfg->K) * elem,
                    box_k, ep::BM))
@@ -288,7 +291,8 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
         return cuda_status(ep::launch_gemm_send_bf16_pair(ta, tb, p, max_pairs, s));
     }
     return cuda_status(fp8 ? ep::launch_gemm_send_fp8(ta, tb, p, bn, grid, s)
-                           : ep::launch_gemm_send_bf16(ta, tb, p, bn, grid, s));
+                           : ep::launch_gemm_send_bf16(ta, tb, p, bn, cfg->send_warps, grid,
+                                                       s));
 }
 
 int ep_combine_reduce(const ep_config *cfg, const ep_combine_args *a, ep_stream_t stream)

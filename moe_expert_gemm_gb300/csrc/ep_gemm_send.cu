@@ -33,34 +33,52 @@
 
 namespace ep {
 
-template <int BN, int STAGES>
+// A staging slot's row destinations, handed with the slot from an epilogue warp to
+// its send warp.
+struct SendSlotMeta {
+    unsigned long long row_base[32];
+    int col_byte;
+    int pad[3];
+};
+
+// SEND = 0: the output warps store their rows themselves. SEND = 4: four dedicated
+// send warps ("EpiloguePeerSink" SendWarps), one per output warp, drain two staging
+// slots per output warp, so that reading TMEM and rounding the next 64 columns
+// overlaps the stores of the previous ones.
+template <int BN, int STAGES, int SEND>
 struct GemmLayout {
     static constexpr int kABytes = BM * kRowBytesK;
     static constexpr int kBBytes = BN * kRowBytesK;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kEpiWarps = 4;
+    static constexpr int kSlots = SEND ? 2 : 1;    // staging slots per output warp
     static constexpr int kWarpStaging = 32 * 128;  // 32 rows x 64 bf16 columns
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + STAGES * kABytes;
     static constexpr int kOffStaging = kOffB + STAGES * kBBytes;
-    static constexpr int kOffBars = kOffStaging + kEpiWarps * kWarpStaging;
-    static constexpr int kNumBars = 2 * STAGES + 5;  // full, empty, acc_full x2, acc_empty x2, mma_done
+    static constexpr int kOffMeta = kOffStaging + kEpiWarps * kSlots * kWarpStaging;
+    static constexpr int kOffBars =
+        kOffMeta + (SEND ? kEpiWarps * kSlots * static_cast<int>(sizeof(SendSlotMeta)) : 0);
+    // full, empty, acc_full x2, acc_empty x2, mma_done (+ slot_full, slot_empty per slot)
+    static constexpr int kNumBars = 2 * STAGES + 5 + (SEND ? 2 * kEpiWarps * kSlots : 0);
     static constexpr int kOffSink = (kOffBars + kNumBars * 8 + 15) / 16 * 16;
     static constexpr int kEnd = kOffSink + static_cast<int>(sizeof(SinkShared));
     static constexpr int kSmemBytes = kEnd + 1024;  // slack to align the base to 1024
     static constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators
-    static constexpr int kThreads = 224;            // TMA, MMA, 4 epilogue, completion
+    // TMA, MMA, 4 output warps, completion (+ send warps)
+    static constexpr int kThreads = 224 + 32 * SEND;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM columns");
+    static_assert(SEND == 0 || SEND == kEpiWarps, "send warps: none, or one per output warp");
 };
 
-template <int BN, int STAGES>
-__global__ void __launch_bounds__(224, 1)
+template <int BN, int STAGES, int SEND>
+__global__ void __launch_bounds__(224 + 32 * SEND, 1)
     gemm_send_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a,
                           const __grid_constant__ CUtensorMap tmap_b,
                           const __grid_constant__ SendParams p)
 {
-    using L = GemmLayout<BN, STAGES>;
+    using L = GemmLayout<BN, STAGES, SEND>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -72,6 +90,9 @@ __global__ void __launch_bounds__(224, 1)
     uint64_t *acc_full = bars + 2 * STAGES;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *mma_done = acc_empty + 2;
+    uint64_t *slot_full = mma_done + 1;  // [output warp][slot], SEND only
+    uint64_t *slot_empty = slot_full + L::kEpiWarps * L::kSlots;
+    SendSlotMeta *meta = reinterpret_cast<SendSlotMeta *>(smem + L::kOffMeta);
     SinkShared *sh = reinterpret_cast<SinkShared *>(smem + L::kOffSink);
     volatile int *abort_flag = &sh->abort_flag;
     const int El = p.El;
@@ -87,6 +108,12 @@ __global__ void __launch_bounds__(224, 1)
             mbar_init(&acc_empty[a], L::kEpiWarps);
         }
         mbar_init(mma_done, 1);
+        if (SEND) {
+            for (int j = 0; j < L::kEpiWarps * L::kSlots; ++j) {
+                mbar_init(&slot_full[j], 1);
+                mbar_init(&slot_empty[j], 1);
+            }
+        }
         fence_mbar_init();
     }
     sink_prologue(p, sh);
@@ -195,13 +222,16 @@ __global__ void __launch_bounds__(224, 1)
         // --------------------------------------------------- epilogue + sink
         const int q = warp & 3;  // TMEM lane quarter this warp may read
         const int epi_tid = threadIdx.x - 64;
-        const uint32_t stg = smem_u32(smem + L::kOffStaging + (warp - 2) * L::kWarpStaging);
+        const uint32_t stg =
+            smem_u32(smem + L::kOffStaging + (warp - 2) * L::kSlots * L::kWarpStaging);
         uint64_t *trace = epi_tid == 0 ? trace_block(p) : nullptr;
         if (trace)
             trace[1] = globaltimer_ns();
 
         bool ok = true;
         bool push_ok = true;  // epi_tid 0: the last hand-off to the completion warp succeeded
+                              // (SEND: every wait of this warp for a free slot succeeded)
+        int k_sub = 0;        // SEND: sub-tiles this warp has handed to its send warp
         int i = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++i) {
             const TileCoord c = decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks, BM, p.m_fastest);
@@ -233,6 +263,17 @@ __global__ void __launch_bounds__(224, 1)
                 tmem_ld_wait();
                 tmem_regs_ready(v0);
                 tmem_regs_ready(v1);
+                const int col_byte = (c.nb * BN + sub * 64) * 2;
+                uint32_t buf = stg;
+                int slot = 0;
+                if constexpr (SEND != 0) {
+                    // wait until the send warp has drained this slot's previous contents
+                    slot = (warp - 2) * L::kSlots + (k_sub % L::kSlots);
+                    buf = stg + (k_sub % L::kSlots) * L::kWarpStaging;
+                    const uint32_t sph = (k_sub / L::kSlots) & 1;
+                    push_ok = mbar_wait(&slot_empty[slot], sph ^ 1u, p.timeout_ns, abort_flag) &&
+                              push_ok;
+                }
                 // fp32 -> bf16 (nearest even), this thread's row, 8 chunks of 16 bytes
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
@@ -244,12 +285,22 @@ __global__ void __launch_bounds__(224, 1)
                             make_float2(__uint_as_float(v[2 * h]), __uint_as_float(v[2 * h + 1])));
                         w[h] = *reinterpret_cast<uint32_t *>(&b);
                     }
-                    st_shared_v4(stg + lane * 128 + ((ch ^ (lane & 7)) << 4),
+                    st_shared_v4(buf + lane * 128 + ((ch ^ (lane & 7)) << 4),
                                  make_uint4(w[0], w[1], w[2], w[3]));
+                }
+                if constexpr (SEND != 0) {
+                    // hand the slot, with its rows' destinations, to the send warp
+                    meta[slot].row_base[lane] = reinterpret_cast<unsigned long long>(row_base);
+                    if (lane == 0)
+                        meta[slot].col_byte = col_byte;
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&slot_full[slot]);
+                    ++k_sub;
+                    continue;
                 }
                 __syncwarp();
                 // 8 lanes per row: each row's 128 bytes leave as one contiguous segment
-                const int col_byte = (c.nb * BN + sub * 64) * 2;
 #pragma unroll
                 for (int it = 0; it < 8; ++it) {
                     const int row = it * 4 + (lane >> 3);
@@ -268,7 +319,11 @@ __global__ void __launch_bounds__(224, 1)
             if (lane == 0)
                 mbar_arrive(&acc_empty[as]);
 
-            if (p.sink_enabled) {
+            if (SEND != 0) {
+                // the send warps hand the tile to the completion warp; a failed wait
+                // for a slot is voted on at the next tile (or reported after the loop)
+                push_ok = __all_sync(0xffffffffu, push_ok);
+            } else if (p.sink_enabled) {
                 // all 128 sink threads' stores of this tile precede the hand-off to the
                 // completion warp, which counts the tile; a failed hand-off is voted
                 // on at the next tile (or reported after the loop)
@@ -286,17 +341,74 @@ __global__ void __launch_bounds__(224, 1)
         if (epi_tid == 0) {
             if (trace)
                 trace[0] = static_cast<uint64_t>(i);
-            close_queue(sh);
-            if (!push_ok)
-                raise_abort(p.status, abort_flag);
+            if (SEND == 0)
+                close_queue(sh);
         }
-        if (!ok && lane == 0)
+        if ((!ok || !push_ok) && lane == 0)
             raise_abort(p.status, abort_flag);
-    } else {
+    } else if (warp == 6) {
         // ------------------------------------------- completion counting + signalling
         if (lane == 0 && p.sink_enabled)
             completion_loop(p, sh);
         __syncwarp();
+    } else if constexpr (SEND != 0) {
+        // ------------------------------------------------------------ send warps
+        // Send warp sw drains the slots of output warp sw in order: each row's 128
+        // bytes of a sub-tile leave as one contiguous segment (8 lanes per row). After
+        // a tile's last sub-tile the send warps meet at a barrier, which is also their
+        // vote, and one thread hands the tile to the completion warp.
+        const int sw = warp - 7;
+        const int send_tid = threadIdx.x - 224;
+        uint64_t *trace = send_tid == 0 ? trace_block(p) : nullptr;
+        bool ok = true;
+        bool push_ok = true;  // send_tid 0: the last hand-off succeeded
+        int k = 0;
+        int i = 0;
+        for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++i) {
+            const TileCoord c =
+                decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks, BM, p.m_fastest);
+            for (int sub = 0; sub < BN / 64; ++sub, ++k) {
+                const int slot = sw * L::kSlots + (k % L::kSlots);
+                const uint32_t sph = (k / L::kSlots) & 1;
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&slot_full[slot], sph, p.timeout_ns, abort_flag));
+                if (!ok)
+                    break;
+                const uint32_t buf = smem_u32(smem + L::kOffStaging + slot * L::kWarpStaging);
+                const int col_byte = meta[slot].col_byte;
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int row = it * 4 + (lane >> 3);
+                    const int ch = lane & 7;
+                    const unsigned long long base = meta[slot].row_base[row];
+                    const uint4 val = ld_shared_v4(buf + row * 128 + ((ch ^ (row & 7)) << 4));
+                    if (base != 0ull)
+                        st_global_v4(reinterpret_cast<uint8_t *>(base) + col_byte + ch * 16, val);
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&slot_empty[slot]);
+            }
+            // every send thread's stores of this tile precede the hand-off
+            ok = named_bar_and(3, 32 * SEND, ok && push_ok);
+            if (!ok)
+                break;
+            if (send_tid == 0) {
+                uint64_t *rec = (trace && i < p.trace_records) ? trace + 2 + 4 * i : nullptr;
+                if (p.sink_enabled) {
+                    if (rec)
+                        rec[2] = globaltimer_ns();
+                    const int tiles_e = (c.m_end - sh->eoff[c.e] + BM - 1) / BM * p.n_blocks;
+                    push_ok = push_tile_done(p, sh, c.e, rec ? i : -1, tiles_e);
+                } else if (rec) {
+                    rec[2] = rec[3] = globaltimer_ns();
+                }
+            }
+        }
+        if (send_tid == 0)
+            close_queue(sh);
+        if ((!ok || !push_ok) && lane == 0)
+            raise_abort(p.status, abort_flag);
     }
 
     // --------------------------------------------------------------- teardown
@@ -308,12 +420,12 @@ __global__ void __launch_bounds__(224, 1)
     }
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int SEND>
 static cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const SendParams &p,
                              int grid, cudaStream_t s)
 {
-    using L = GemmLayout<BN, STAGES>;
-    auto kern = gemm_send_bf16_kernel<BN, STAGES>;
+    using L = GemmLayout<BN, STAGES, SEND>;
+    auto kern = gemm_send_bf16_kernel<BN, STAGES, SEND>;
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (err != cudaSuccess)
@@ -323,15 +435,29 @@ static cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const
 }
 
 cudaError_t launch_gemm_send_bf16(const CUtensorMap &ta, const CUtensorMap &tb,
-                                  const SendParams &p, int bn, int grid, cudaStream_t s)
+                                  const SendParams &p, int bn, int send_warps, int grid,
+                                  cudaStream_t s)
 {
+    if (send_warps == 4) {
+        // the second staging slot of each output warp takes the room of one stage
+        switch (bn) {
+        case 256:
+            return launch_bn<256, 3, 4>(ta, tb, p, grid, s);
+        case 128:
+            return launch_bn<128, 5, 4>(ta, tb, p, grid, s);
+        case 64:
+            return launch_bn<64, 7, 4>(ta, tb, p, grid, s);
+        default:
+            return cudaErrorInvalidValue;
+        }
+    }
     switch (bn) {
     case 256:
-        return launch_bn<256, 4>(ta, tb, p, grid, s);
+        return launch_bn<256, 4, 0>(ta, tb, p, grid, s);
     case 128:
-        return launch_bn<128, 6>(ta, tb, p, grid, s);
+        return launch_bn<128, 6, 0>(ta, tb, p, grid, s);
     case 64:
-        return launch_bn<64, 8>(ta, tb, p, grid, s);
+        return launch_bn<64, 8, 0>(ta, tb, p, grid, s);
     default:
         return cudaErrorInvalidValue;
     }

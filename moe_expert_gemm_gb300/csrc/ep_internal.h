@@ -63,7 +63,8 @@ struct CombineParams {
 // Kernel launchers; each returns the launch's cudaError_t.
 cudaError_t launch_plan(const PlanParams &p, cudaStream_t s);
 cudaError_t launch_gemm_send_bf16(const CUtensorMap &ta, const CUtensorMap &tb,
-                                  const SendParams &p, int bn, int grid, cudaStream_t s);
+                                  const SendParams &p, int bn, int send_warps, int grid,
+                                  cudaStream_t s);
 cudaError_t launch_gemm_send_fp8(const CUtensorMap &ta, const CUtensorMap &tb,
                                  const SendParams &p, int bn, int grid, cudaStream_t s);
 cudaError_t launch_gemm_send_bf16_pair(const CUtensorMap &ta, const CUtensorMap &tb,

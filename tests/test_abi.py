@@ -101,6 +101,13 @@ def test_fp8_shape_rules(lib):
             ep.EP_ERR_UNSUPPORTED
 
 
+def test_fp8_has_no_dedicated_send_warps(lib):
+    """Dedicated send warps exist in the bf16 kernel only."""
+    cfg = _cfg(dtype=ep.EP_FP8_1D2D, send_warps=4)
+    assert lib.grouped_gemm_combine_send(ctypes.byref(cfg), ctypes.byref(ep.ep_send_args()),
+                                         None) == ep.EP_ERR_UNSUPPORTED
+
+
 def test_strerror(lib):
     assert ep.ep_strerror(ep.EP_ERR_UNSUPPORTED) == "unsupported configuration"
     assert "timed out" in ep.ep_strerror(ep.EP_STATUS_TIMEOUT)

@@ -19,9 +19,9 @@ from synth import Routing, Workload, WORKLOADS, make_routing
 pytestmark = pytest.mark.gpu
 
 
-def _check_full(w, routing=None, values=None, epoch=3):
+def _check_full(w, routing=None, values=None, epoch=3, send_warps=-1):
     routing, values = (routing, values) if values is not None else make_inputs(w, routing)
-    s = build_system(w, routing, values)
+    s = build_system(w, routing, values, send_warps=send_warps)
     run_all(s, epoch)
     torch.cuda.synchronize()
     st = s.status_words()
@@ -140,11 +140,12 @@ def test_identity_weights_bit_exact(T):
                                       ref["out"][d])
 
 
-def test_local_store_when_sink_disabled():
+@pytest.mark.parametrize("send_warps", [-1, 4])
+def test_local_store_when_sink_disabled(send_warps):
     """p3_control < 0: rows go to the local C in plan order, nothing is sent or signalled."""
     w = WORKLOADS["tiny"]
     routing, values = make_inputs(w)
-    s = build_system(w, routing, values)
+    s = build_system(w, routing, values, send_warps=send_warps)
     r = 1
     m = s.plan_host(r)["m_total"]
     C = torch.zeros((s.ops[r]["A"].shape[0], w.N), dtype=torch.bfloat16, device="cuda")
@@ -161,15 +162,17 @@ def test_local_store_when_sink_disabled():
     assert max_rel_err(got, Y) <= TOL["bf16"]
 
 
-@pytest.mark.parametrize("N,T,pair", [(384, 300, False), (512, 600, True)])
-def test_trace_records_every_tile_once(N, T, pair):
+@pytest.mark.parametrize("N,T,pair,send_warps", [(384, 300, False, -1), (512, 600, True, -1),
+                                                 (512, 600, False, 4)])
+def test_trace_records_every_tile_once(N, T, pair, send_warps):
     """Optional per-tile timestamps: every tile appears once per CTA that works on
     it (single CTAs: once; 256-column bf16 tiles on CTA pairs: once per CTA of the
     pair), times are ordered, and exactly the non-empty experts are marked as
-    completed, once each."""
+    completed, once each. With dedicated send warps the stored time is taken by
+    the send warps, after the output warps have handed over every sub-tile."""
     w = Workload("trace_small", 4, 4, 2, T, 256, N, "bf16", "zipf", "softmax_sel", 50)
     routing, values = make_inputs(w)
-    s = build_system(w, routing, values)
+    s = build_system(w, routing, values, send_warps=send_warps)
     for r in range(w.n_ranks):
         s.send(r, epoch=1)
     tr = s.send_traced(1, epoch=2, records=64)
@@ -178,7 +181,8 @@ def test_trace_records_every_tile_once(N, T, pair):
     assert sum(b["tiles"] for b in tr) == len(recs)
     pl = oracle.plan(w.n_ranks, w.n_local_experts, w.top_k, routing.topk_ids, 1)
     rows = np.diff(pl.expert_offsets)
-    tile_rows, n_blocks, copies = (256, N // 256, 2) if pair else (128, N // 128, 1)
+    bn = 256 if N % 256 == 0 else (128 if N % 128 == 0 else 64)  # widest column block
+    tile_rows, n_blocks, copies = (256, N // bn, 2) if pair else (128, N // bn, 1)
     n_tiles = int((-(-rows // tile_rows)).sum()) * n_blocks
     assert sorted(r["tile"] for r in recs) == sorted(list(range(n_tiles)) * copies)
     assert all(b["t_start"] <= r["t_ready"] <= r["t_stored"] <= r["t_done"]
@@ -200,3 +204,44 @@ def test_fp8_many_rows_per_expert_parity():
     scale blocks along K and N."""
     w = Workload("fp8_pair_small", 2, 2, 2, 400, 384, 512, "fp8_1d2d", "zipf", "sigmoid_sel", 56)
     _check_full(w)
+
+
+SEND_WARP_CASES = [
+    # 256-, 128- and 64-column tiles; ragged tails; empty experts; eight ranks; a
+    # shape that would otherwise run on CTA pairs
+    ("tiny", WORKLOADS["tiny"]),
+    ("bn256_ragged", Workload("sw256", 4, 2, 2, 100, 256, 256, "bf16", "uniform",
+                              "softmax_sel", 60)),
+    ("bn128_eight_ranks", Workload("sw128", 8, 1, 2, 40, 128, 384, "bf16", "biased",
+                                   "softmax_sel", 61)),
+    ("bn64_single_rank", Workload("sw64", 1, 3, 1, 77, 192, 192, "bf16", "uniform",
+                                  "softmax_sel", 62)),
+    ("pair_shape", Workload("sw_pair", 4, 3, 2, 400, 320, 512, "bf16", "zipf",
+                            "softmax_sel", 63)),
+    ("qwen_shape_small", Workload("sw_qwen", 8, 16, 8, 48, 1536, 4096, "bf16", "zipf",
+                                  "softmax_sel", 64)),
+]
+
+
+@pytest.mark.parametrize("name,w", SEND_WARP_CASES, ids=[c[0] for c in SEND_WARP_CASES])
+def test_dedicated_send_warps_parity(name, w):
+    """send_warps = 4: four send warps, one per output warp, store the rows the
+    output warps stage in two slots each. Same plans, counts, flags, rows and
+    combined outputs as the inline sink; counters re-armed."""
+    _check_full(w, send_warps=4)
+
+
+def test_dedicated_send_warps_two_epochs_and_empty_experts():
+    w = Workload("sw_empty", 4, 4, 2, 30, 256, 512, "bf16", "uniform", "softmax_sel", 65)
+    rng = np.random.default_rng(10)
+    choices = np.array([0, 5, 6, 13], np.int32)
+    ids = np.stack([np.stack([rng.choice(choices, 2, replace=False) for _ in range(w.tokens)])
+                    for _ in range(w.n_ranks)])
+    routing = _fixed_routing(w, ids)
+    s, ref, routing, values = _check_full(w, routing, epoch=5, send_warps=4)
+    run_all(s, 6)
+    torch.cuda.synchronize()
+    assert (s.status_words() == 0).all()
+    ref2 = full_pipeline(w, routing, values, epoch=6)
+    for d in range(w.n_ranks):
+        np.testing.assert_array_equal(s.counts[d].cpu().numpy().view(np.uint64), ref2["counts"][d])
