@@ -245,3 +245,45 @@ def test_dedicated_send_warps_two_epochs_and_empty_experts():
     ref2 = full_pipeline(w, routing, values, epoch=6)
     for d in range(w.n_ranks):
         np.testing.assert_array_equal(s.counts[d].cpu().numpy().view(np.uint64), ref2["counts"][d])
+
+
+FP8_ROW_BLOCK_CASES = [
+    # several 128-row blocks per expert with ragged last blocks; zipf routing leaves
+    # experts empty; 256- and 128-column tiles
+    ("bn256_zipf_empty", Workload("fp8_rb_zipf", 4, 4, 4, 300, 256, 768, "fp8_1d2d", "zipf",
+                                  "sigmoid_sel", 57)),
+    ("bn128_ragged", Workload("fp8_rb_128", 2, 2, 2, 300, 256, 384, "fp8_1d2d", "uniform",
+                              "sigmoid_sel", 58)),
+]
+
+
+@pytest.mark.parametrize("name,w", FP8_ROW_BLOCK_CASES, ids=[c[0] for c in FP8_ROW_BLOCK_CASES])
+def test_fp8_row_block_parity(name, w):
+    _check_full(w)
+
+
+@pytest.mark.parametrize("T", [100, 600])  # one / several row blocks per expert
+def test_fp8_identity_weights_bit_exact(T):
+    """Blockwise fp8 with W_e = I (e4m3 1.0 on the diagonal), power-of-two scales,
+    top_k = 1, gate 1: y[m, n] = sa[m, n/128] * sw[e, n/128, n/128] * a8[m, n] is
+    exact in bf16, so rows and combined outputs match the oracle bit for bit."""
+    w = Workload("ident_fp8", 4, 2, 1, T, 256, 256, "fp8_1d2d", "uniform", "softmax_indep", 59)
+    routing, values = make_inputs(w)
+    routing.gates[:] = 1.0
+    rng = np.random.default_rng(11)
+    for q in range(w.n_ranks):
+        v = values[q]
+        v["W"] = np.zeros_like(v["W"])
+        for e in range(w.n_local_experts):
+            np.fill_diagonal(v["W"][e], 0x38)  # e4m3 1.0
+        v["a_scales"] = np.exp2(rng.integers(-4, 5, v["a_scales"].shape)).astype(np.float32)
+        v["w_scales"] = np.exp2(rng.integers(-4, 5, v["w_scales"].shape)).astype(np.float32)
+    s = build_system(w, routing, values)
+    run_all(s, 1)
+    torch.cuda.synchronize()
+    assert (s.status_words() == 0).all()
+    ref = full_pipeline(w, routing, values, epoch=1)
+    for d in range(w.n_ranks):
+        np.testing.assert_array_equal(s.recv[d].cpu().numpy(), ref["recv"][d])
+        np.testing.assert_array_equal(s.out[d].view(torch.int16).cpu().numpy().view(np.uint16),
+                                      ref["out"][d])

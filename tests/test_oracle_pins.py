@@ -417,6 +417,37 @@ def test_identity_weights_move_data_exactly():
                                           a * 2.0**(e + 1 - q))
 
 
+def test_fp8_identity_weights_move_data_exactly():
+    """Blockwise fp8, K = N, W_e = I (e4m3 1.0), power-of-two scales, top_k = 1,
+    gate 1: out[t, n] = sa[row, n/128] * sw[e, n/128, n/128] * a8[row, n] exactly
+    (a dropped or transposed scale index changes the result)."""
+    w = Workload("ident8", 2, 2, 1, 20, 256, 256, "fp8_1d2d", "uniform", "softmax_indep", 92)
+    r = make_routing(w)
+    r.gates[:] = 1.0
+    m = rows_per_rank(w, r.topk_ids)
+    rng = np.random.default_rng(3)
+    vals = []
+    for q in range(w.n_ranks):
+        v = make_rank_values(w, q, int(m[q]))
+        v["W"] = np.zeros_like(v["W"])
+        for e in range(w.n_local_experts):
+            np.fill_diagonal(v["W"][e], 0x38)
+        v["a_scales"] = np.exp2(rng.integers(-4, 5, v["a_scales"].shape)).astype(np.float32)
+        v["w_scales"] = np.exp2(rng.integers(-4, 5, v["w_scales"].shape)).astype(np.float32)
+        vals.append(v)
+    res = full_pipeline(w, r, vals, epoch=1)
+    keys = {q: _brute_plan(r.topk_ids, w.n_ranks, w.n_local_experts, q) for q in range(w.n_ranks)}
+    n_blk = np.arange(w.N) // 128
+    for d in range(w.n_ranks):
+        for t in range(w.tokens):
+            g = int(r.topk_ids[d, t, 0])
+            q, e = g // w.n_local_experts, g % w.n_local_experts
+            row = keys[q].index((e, d, t, 0))
+            a8 = torch.from_numpy(vals[q]["A"][row]).view(torch.float8_e4m3fn).double().numpy()
+            want = a8 * vals[q]["a_scales"][row, n_blk] * vals[q]["w_scales"][e, n_blk, n_blk]
+            np.testing.assert_array_equal(oracle.bf16_to_f64(res["out"][d][t]), want)
+
+
 def test_sampled_pipeline_agrees_with_full():
     w, r, vals, res = _tiny_full()
     toks = np.array([0, 5, 63, 17])
