@@ -17,7 +17,8 @@
 
 namespace ep {
 
-constexpr int kQueue = 64;  // finished-tile queue, epilogue -> completion warp
+constexpr int kQueue = 64;        // finished-tile queue, epilogue -> completion warp
+constexpr int kCountCache = 512;  // send counts kept in shared memory when E_l * R fits
 
 // Shared-memory state of the sink, one per thread block.
 struct SinkShared {
@@ -25,7 +26,8 @@ struct SinkShared {
     uint64_t *cnt[EP_MAX_RANKS];
     int tile_start[EP_MAX_LOCAL_EXPERTS + 1];
     int eoff[EP_MAX_LOCAL_EXPERTS + 1];
-    int4 queue[kQueue];  // {expert, trace record or -1, tiles of the expert, 0}
+    int counts[kCountCache];  // send_counts[e * R + dst], when E_l * R <= kCountCache
+    int4 queue[kQueue];       // {expert, trace record or -1, tiles of the expert, 0}
     int q_head, q_tail, q_done, abort_flag;
     uint32_t tmem_slot;
 };
@@ -36,27 +38,45 @@ __device__ __forceinline__ void raise_abort(uint32_t *status, volatile int *abor
     *abort_flag = 1;
 }
 
-// Completion signalling of local expert e towards every destination rank. The
-// caller has acquired every row of expert e. For each destination: a plain
-// progress store of the count word, then the election on that destination's
-// counter. The release half of the acquire-release election is one system-scope
-// fence ahead of all R increments (it releases the rows and the count words); the
-// acquire half is a second fence, taken only when this call is elected for some
-// destination, which also orders the rank-flag stores after everything the other
-// experts released.
-static __device__ __noinline__ void signal_expert(const SendParams &p, int e, uint64_t *const *cnt)
+// Completion signalling ("ep_signal_completion", ep_ord_r with has_rank_flag) is
+// split in three steps so that the completion of the last expert, which ends the
+// call, waits on as few fences as possible:
+//  1. store_counts: the plain progress stores of expert e's count words, one per
+//     destination (values from shared memory, so no load sits between them);
+//  2. the caller's system-scope acquire-release fence: it acquires the expert's
+//     other tiles (whose rows the other blocks released before their tile-counter
+//     increments) and releases every row and count word of the expert to the peers;
+//  3. elect_and_publish: the increments of the per-destination election counters
+//     (this GPU's memory, updated only by this GPU's blocks, so gpu-scope RMWs);
+//     the block that makes a counter reach E_l has acquired every other expert's
+//     release through that RMW chain, takes one more system-scope fence, re-arms
+//     the counter and publishes the rank flag.
+__device__ __forceinline__ void store_counts(const SendParams &p, const SinkShared *sh, int e)
 {
     const int R = p.n_ranks;
-    for (int dst = 0; dst < R; ++dst) {
-        volatile uint64_t *w = cnt[dst] + static_cast<int64_t>(e) * R + p.my_rank;
-        *w = static_cast<uint64_t>(p.send_counts[e * R + dst]);
+    const bool cached = p.El * R <= kCountCache;
+    int c[EP_MAX_RANKS];
+#pragma unroll
+    for (int dst = 0; dst < EP_MAX_RANKS; ++dst)
+        c[dst] = dst < R ? (cached ? sh->counts[e * R + dst] : __ldg(p.send_counts + e * R + dst))
+                         : 0;
+#pragma unroll
+    for (int dst = 0; dst < EP_MAX_RANKS; ++dst) {
+        if (dst < R) {
+            volatile uint64_t *w = sh->cnt[dst] + static_cast<int64_t>(e) * R + p.my_rank;
+            *w = static_cast<uint64_t>(c[dst]);
+        }
     }
-    fence_acq_rel_sys();
+}
+
+static __device__ __noinline__ void elect_and_publish(const SendParams &p, const SinkShared *sh)
+{
+    const int R = p.n_ranks;
     int old[EP_MAX_RANKS];
 #pragma unroll
     for (int dst = 0; dst < EP_MAX_RANKS; ++dst)
         if (dst < R)
-            old[dst] = atom_add_relaxed_sys(&p.rank_counter[dst], 1);
+            old[dst] = atom_add_relaxed_gpu(&p.rank_counter[dst], 1);
     bool elected = false;
 #pragma unroll
     for (int dst = 0; dst < EP_MAX_RANKS; ++dst)
@@ -70,7 +90,8 @@ static __device__ __noinline__ void signal_expert(const SendParams &p, int e, ui
             // last expert of this rank for dst: re-arm the counter for the next call and
             // publish the whole rank through the rank flag
             *reinterpret_cast<volatile int *>(&p.rank_counter[dst]) = 0;
-            st_relaxed_sys_u64(cnt[dst] + static_cast<int64_t>(p.El) * R + p.my_rank, p.epoch);
+            st_relaxed_sys_u64(sh->cnt[dst] + static_cast<int64_t>(p.El) * R + p.my_rank,
+                               p.epoch);
         }
     }
 }
@@ -133,6 +154,9 @@ __device__ __forceinline__ void sink_prologue(const SendParams &p, SinkShared *s
     }
     for (int e = threadIdx.x; e <= El; e += blockDim.x)
         sh->eoff[e] = __ldg(p.expert_offsets + e);
+    if (p.sink_enabled && El * p.n_ranks <= kCountCache)
+        for (int i = threadIdx.x; i < El * p.n_ranks; i += blockDim.x)
+            sh->counts[i] = __ldg(p.send_counts + i);
     __syncthreads();
     if (threadIdx.x == 32) {
         int prev = 0;
@@ -213,9 +237,10 @@ __device__ __forceinline__ void close_queue(SinkShared *sh)
 }
 
 // Completion warp, one thread: counts finished tiles per expert (one gpu-scope
-// release fence per batch of tiles, acquire fence when an expert completes) and
-// runs the signalling of every expert this block completes. Block 0 also
-// signals the experts without rows, which have no tile to complete.
+// release fence per batch of tiles) and runs the signalling of every expert this
+// block completes (count stores, one system-scope acquire-release fence for the
+// batch, election). Block 0 also signals the experts without rows, which have no
+// tile to complete.
 static __device__ void completion_loop(const SendParams &p, SinkShared *sh)
 {
     volatile int *head_p = &sh->q_head;
@@ -224,9 +249,19 @@ static __device__ void completion_loop(const SendParams &p, SinkShared *sh)
     volatile int *abort_flag = &sh->abort_flag;
     uint64_t *trace = trace_block(p);
     if (blockIdx.x == 0) {
-        for (int e = 0; e < p.El; ++e)
-            if (sh->eoff[e + 1] == sh->eoff[e])
-                signal_expert(p, e, sh->cnt);
+        bool any_empty = false;
+        for (int e = 0; e < p.El; ++e) {
+            if (sh->eoff[e + 1] == sh->eoff[e]) {
+                store_counts(p, sh, e);
+                any_empty = true;
+            }
+        }
+        if (any_empty) {
+            fence_acq_rel_sys();
+            for (int e = 0; e < p.El; ++e)
+                if (sh->eoff[e + 1] == sh->eoff[e])
+                    elect_and_publish(p, sh);
+        }
     }
     int head = 0;
     uint64_t t0 = globaltimer_ns();
@@ -249,12 +284,17 @@ static __device__ void completion_loop(const SendParams &p, SinkShared *sh)
                 last[j] = old == ent[j].z - 1;
                 any |= last[j];
             }
-            if (any)
-                fence_acq_rel_gpu();  // acquire the expert's other tiles
+            if (any) {
+                for (int j = 0; j < n; ++j)
+                    if (last[j])
+                        store_counts(p, sh, ent[j].x);
+                // acquire the experts' other tiles; release their rows and counts
+                fence_acq_rel_sys();
+            }
             for (int j = 0; j < n; ++j) {
                 if (last[j]) {
                     *reinterpret_cast<volatile int *>(&p.atomic_counter[ent[j].x]) = 0;
-                    signal_expert(p, ent[j].x, sh->cnt);
+                    elect_and_publish(p, sh);
                 }
                 if (trace && ent[j].y >= 0) {
                     uint64_t *rec = trace + 2 + 4 * ent[j].y;
