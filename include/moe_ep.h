@@ -114,6 +114,8 @@ typedef struct {
  *   m_total        [1]           row count
  *   status         [1]           EP_STATUS_* bits (OR-ed)
  * max_rows is the capacity of src_info / gather_idx (and of the A operand).
+ * src_info is read and written as 8-byte pairs: it must be 8-byte aligned, else
+ * EP_ERR_INVALID_ARG (here and in grouped_gemm_combine_send).
  */
 typedef struct {
     int32_t *expert_offsets;

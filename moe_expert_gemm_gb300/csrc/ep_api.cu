@@ -154,6 +154,8 @@ int ep_plan(const ep_config *cfg, const int32_t *topk_ids, const ep_plan_out *ou
         return EP_ERR_INVALID_ARG;
     if (out->max_rows < 0 || out->max_rows > INT32_MAX)
         return EP_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(out->src_info) & 7u)
+        return EP_ERR_INVALID_ARG;  // written as (src_idx, src_topk) pairs
     ep::PlanParams p;
     p.n_ranks = cfg->n_ranks;
     p.my_rank = cfg->my_rank;
@@ -202,6 +204,8 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
         return EP_ERR_INVALID_ARG;
     if (!aligned16(a->A) || !aligned16(a->W))
         return EP_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(a->src_info) & 7u)
+        return EP_ERR_INVALID_ARG;  // read as (src_idx, src_topk) pairs
     if (a->max_rows < 1 || a->max_rows > INT32_MAX)
         return EP_ERR_INVALID_ARG;
     if (sink) {

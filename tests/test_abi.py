@@ -92,6 +92,25 @@ def test_unaligned_operand_rejected(lib):
         ep.EP_ERR_INVALID_ARG
 
 
+def test_unaligned_src_info_rejected(lib):
+    """src_info is accessed as 8-byte (src_idx, src_topk) pairs."""
+    cfg = _cfg()
+    out = ep.ep_plan_out(0x1000, 0x2000004, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 64)
+    assert lib.ep_plan(ctypes.byref(cfg), ctypes.c_void_p(0x8000), ctypes.byref(out),
+                       None) == ep.EP_ERR_INVALID_ARG
+    a = ep.ep_send_args()
+    a.A, a.W = 0x1000000, 0x2000000
+    a.expert_offsets = a.seg_offsets = a.send_counts = a.status = 0x3000000
+    a.src_info = 0x3000004
+    a.max_rows = 8
+    for r in range(4):
+        a.recv_buf_ptrs[r] = 0x4000000 + r * 0x100000
+        a.recv_count_ptrs[r] = 0x5000000 + r * 0x100000
+    a.atomic_counter = a.rank_completion_counter = 0x6000000
+    assert lib.grouped_gemm_combine_send(ctypes.byref(cfg), ctypes.byref(a), None) == \
+        ep.EP_ERR_INVALID_ARG
+
+
 def test_fp8_shape_rules(lib):
     """Blockwise fp8 needs whole 128-wide scale blocks along K and N."""
     a = ep.ep_send_args()
