@@ -139,15 +139,20 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+# Sources that decide what the fused GEMM+send kernels do on the device: the kernels,
+# their shared headers, and the host code that picks the kernel, tile and tile order.
+FUSED_KERNEL_SOURCES = ("ep_api.cu", "ep_gemm_send.cu", "ep_gemm_send_fp8.cu",
+                        "ep_gemm_send_pair.cu", "ep_internal.h", "ep_ptx.cuh", "ep_sink.cuh")
+
+
 def kernel_source_sha() -> str:
-    """Digest of every kernel source file (a measurement taken on other sources
+    """Digest of the fused kernels' sources (a measurement taken on other sources
     does not describe the current kernels)."""
     csrc = os.path.join(ROOT, "moe_expert_gemm_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in FUSED_KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
