@@ -65,6 +65,9 @@ def parse_args():
                     help="after timing, run one traced send and write its summary here")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override tokens per rank (profiling a smaller case of a workload)")
+    ap.add_argument("--path", choices=["fused", "unfused"], default="fused",
+                    help="unfused: the comparator without the sink (GEMM rows to a local C, "
+                         "then ep_scatter_send); times the same step")
     ap.add_argument("--send-warps", type=int, default=-1, choices=[-1, 0, 4],
                     help="sink placement: -1 library choice, 0 inside the output warps, "
                          "4 dedicated send warps (bf16)")
@@ -319,6 +322,8 @@ def main():
     flush = torch.empty(512 * 2**20, dtype=torch.uint8, device="cuda") \
         if step_bytes < 2 * L2_BYTES else None
     epoch = [2]
+    unfused = args.path == "unfused"
+    C_local = s.local_C(q) if unfused else None
 
     def one_step(evs=None):
         e = epoch[0]
@@ -329,7 +334,13 @@ def main():
             s.counts[q].index_fill_(0, peer_idx, e)
         if evs is not None:
             evs[0].record(stream)
-        s.send(q, e, stream)
+        if unfused:
+            s.send(q, e, stream, p3_control=-1, C=C_local)
+            if evs is not None:
+                evs[3].record(stream)
+            ep.ep_scatter_send(s.cfg(q), s.scatter_args(q, e, C_local), stream)
+        else:
+            s.send(q, e, stream)
         if evs is not None:
             evs[1].record(stream)
         if not args.solo:
@@ -345,7 +356,7 @@ def main():
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     time.sleep(0.5)  # let the sampler start before the timed region
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     torch.cuda.synchronize()
     for i in range(args.steps):
         one_step(events[i])
@@ -355,6 +366,7 @@ def main():
     clk = clocks.stop()
     send_ms = [e[0].elapsed_time(e[1]) for e in events]
     comb_ms = [e[1].elapsed_time(e[2]) for e in events]
+    gemm_ms = [e[0].elapsed_time(e[3]) for e in events] if unfused else None
     step_ms = sum(a + b for a, b in zip(send_ms, comb_ms)) / args.steps
     st = s.status_words()
     if st.any():
@@ -379,7 +391,7 @@ def main():
     # outputs double-buffered, so step i+1's host->device copies overlap step i's kernels
     # and step i's read-back overlaps step i+1's.
     e2e = None
-    if not args.no_e2e and not args.solo:
+    if not args.no_e2e and not args.solo and not unfused:
         ops = s.ops[q]
         A_bufs = [ops["A"], torch.empty_like(ops["A"])]
         fp8 = "a_scales" in ops
@@ -465,20 +477,23 @@ def main():
     peaks, peak_src = load_peaks()
     send_s = statistics.mean(send_ms) / 1e3
     comb_s = statistics.mean(comb_ms) / 1e3
-    tflops = flops / send_s / 1e12
+    # the dominant kernel: the fused GEMM + send, or (unfused) the GEMM into the local C
+    dom_s = statistics.mean(gemm_ms) / 1e3 if unfused else send_s
+    tflops = flops / dom_s / 1e12
     peak_tf = float(peaks["bf16_tflops"]) * (2.0 if w.dtype == "fp8_1d2d" else 1.0)
     peak_bw = float(peaks["hbm_gbs"])
     t_tensor = flops / (peak_tf * 1e12)
     t_hbm = send_bytes / (peak_bw * 1e9)
-    traffic = measured_traffic(w.name, "grouped_gemm_combine_send")
+    traffic = None if unfused else measured_traffic(w.name, "grouped_gemm_combine_send")
     if t_tensor >= t_hbm:
         roof = {"bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": tflops / peak_tf, "traffic": traffic}
     else:
-        gbs = send_bytes / send_s / 1e9
+        gbs = send_bytes / dom_s / 1e9
         roof = {"bound": "hbm", "achieved": gbs, "peak": peak_bw, "unit": "GB/s",
                 "frac": gbs / peak_bw, "traffic": traffic}
-    roof["kernel"] = "grouped_gemm_combine_send"
+    roof["kernel"] = ("grouped_gemm_combine_send with the sink disabled (rows to a local C)"
+                      if unfused else "grouped_gemm_combine_send")
     roof["peak_source"] = (f"{peak_src}: " + ("bf16_tflops (burst)" if roof["bound"] == "tensor"
                                               else "hbm_gbs")
                            + (" x2 nominal fp8/bf16 ratio" if w.dtype == "fp8_1d2d"
@@ -494,17 +509,20 @@ def main():
         "config": {"workload": w.name, "n_ranks": w.n_ranks, "n_local_experts": w.n_local_experts,
                    "top_k": w.top_k, "tokens_per_rank": w.tokens, "K": w.K, "N": w.N,
                    "operands": w.dtype, "my_rank": q, "rows": m_rows,
-                   "send_warps": args.send_warps,
+                   "send_warps": args.send_warps, "path": args.path,
                    "l2": ("flushed with a 512 MB write before every step" if flush is not None
                           else f"per-step inputs {step_bytes / 1e6:.0f} MB > L2"),
                    "parallelism": "replicas: one logical rank per GPU" if world > 1
                    else "one logical rank"},
         "tflops": tflops,
-        "kernels_ms": {"grouped_gemm_combine_send": statistics.mean(send_ms),
-                       "ep_combine_reduce": statistics.mean(comb_ms)},
+        "kernels_ms": ({"grouped_gemm_combine_send (local C)": statistics.mean(gemm_ms),
+                        "ep_scatter_send": statistics.mean(send_ms) - statistics.mean(gemm_ms),
+                        "ep_combine_reduce": statistics.mean(comb_ms)} if unfused else
+                       {"grouped_gemm_combine_send": statistics.mean(send_ms),
+                        "ep_combine_reduce": statistics.mean(comb_ms)}),
         "combine_gbs": comb_bytes / comb_s / 1e9,
         "roofline": roof,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (3 if unfused else 2) * args.steps,
         "clocks": clk,
     }
     if e2e is not None:

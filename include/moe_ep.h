@@ -258,6 +258,45 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *args,
 int grouped_gemm_combine_send_noalloc(const ep_config *cfg, const ep_send_args *args,
                                       ep_stream_t stream);
 
+/* ------------------------------------------------------- unfused send */
+
+/*
+ * ep_scatter_send -- the send step on its own, for the unfused comparator
+ * ("EpiloguePeerSink" disabled, i.e. the null sink: the grouped GEMM stores its
+ * output tile to the local C, here grouped_gemm_combine_send with p3_control < 0,
+ * and a separate kernel then moves the rows). It reads the local C produced that
+ * way and delivers exactly what the fused call delivers: every row to
+ * (src_idx*top_k + src_topk)*msg_bytes of its destination's receive buffer
+ * ("P3PeerSendConfig"), the count words, and the rank flag of my_rank in every
+ * destination's count buffer ("ep_signal_completion"), the flag after all rows
+ * and counts (one launch sends every expert, so the last thread block to finish
+ * signals all of them at once).
+ *   C                [max_rows][N] bf16, row m = output row m in plan order
+ *   expert_offsets, src_info, seg_offsets, send_counts   the plan (ep_plan)
+ *   max_rows         rows allocated for C (and src_info)
+ *   recv_buf_ptrs, recv_count_ptrs, epoch, status   as for grouped_gemm_combine_send
+ *   block_counter    one int32 in device memory, 0 before the first call; the call
+ *                    that uses it re-arms it to 0
+ * Errors: as for grouped_gemm_combine_send (EP_ERR_INVALID_ARG for NULL or
+ * misaligned pointers, src_info not 8-byte aligned; EP_STATUS_BOUNDS for a row
+ * whose destination lies outside the receive buffer, which is skipped).
+ */
+typedef struct {
+    const void *C;
+    const int32_t *expert_offsets;
+    const int32_t *src_info;
+    const int32_t *seg_offsets;
+    const int32_t *send_counts;
+    int64_t max_rows;
+    void *recv_buf_ptrs[EP_MAX_RANKS];
+    uint64_t *recv_count_ptrs[EP_MAX_RANKS];
+    int32_t *block_counter;
+    uint64_t epoch;
+    uint32_t *status;
+} ep_scatter_args;
+
+int ep_scatter_send(const ep_config *cfg, const ep_scatter_args *args, ep_stream_t stream);
+
 /* --------------------------------------------------------------- combine */
 
 /*

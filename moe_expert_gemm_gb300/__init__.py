@@ -61,6 +61,13 @@ class ep_combine_args(ctypes.Structure):
                 ("epoch", _c_u64), ("timeout_ns", _c_i64), ("status", _vp)]
 
 
+class ep_scatter_args(ctypes.Structure):
+    _fields_ = [("C", _vp), ("expert_offsets", _vp), ("src_info", _vp), ("seg_offsets", _vp),
+                ("send_counts", _vp), ("max_rows", _c_i64),
+                ("recv_buf_ptrs", _vp * EP_MAX_RANKS), ("recv_count_ptrs", _vp * EP_MAX_RANKS),
+                ("block_counter", _vp), ("epoch", _c_u64), ("status", _vp)]
+
+
 class EpError(RuntimeError):
     def __init__(self, code: int, where: str):
         super().__init__(f"{where}: {ep_strerror(code)} ({code})")
@@ -70,7 +77,7 @@ class EpError(RuntimeError):
 _lib = None
 
 EXPORTS = ("ep_plan_sizes", "ep_plan", "grouped_gemm_combine_send", "ep_combine_reduce",
-           "ep_strerror", "grouped_gemm_combine_send_noalloc")
+           "ep_strerror", "grouped_gemm_combine_send_noalloc", "ep_scatter_send")
 
 
 def load(build_if_missing: bool = True):
@@ -91,8 +98,9 @@ def load(build_if_missing: bool = True):
                                     _vp]
     L.grouped_gemm_combine_send_noalloc.argtypes = [ctypes.POINTER(ep_config),
                                                     ctypes.POINTER(ep_send_args), _vp]
+    L.ep_scatter_send.argtypes = [ctypes.POINTER(ep_config), ctypes.POINTER(ep_scatter_args), _vp]
     for f in ("ep_plan_sizes", "ep_plan", "grouped_gemm_combine_send", "ep_combine_reduce",
-              "grouped_gemm_combine_send_noalloc"):
+              "grouped_gemm_combine_send_noalloc", "ep_scatter_send"):
         getattr(L, f).restype = ctypes.c_int
     L.ep_strerror.argtypes = [ctypes.c_int]
     L.ep_strerror.restype = ctypes.c_char_p
@@ -150,6 +158,13 @@ def grouped_gemm_combine_send_noalloc(cfg: ep_config, args: ep_send_args, stream
     return _check(load().grouped_gemm_combine_send_noalloc(ctypes.byref(cfg), ctypes.byref(args),
                                                            stream_handle(stream)),
                   "grouped_gemm_combine_send_noalloc")
+
+
+def ep_scatter_send(cfg: ep_config, args: ep_scatter_args, stream=None) -> int:
+    """The send step alone (unfused comparator): local C rows to the receive
+    buffers, then the count words and the rank flags."""
+    return _check(load().ep_scatter_send(ctypes.byref(cfg), ctypes.byref(args),
+                                         stream_handle(stream)), "ep_scatter_send")
 
 
 def ep_combine_reduce(cfg: ep_config, args: ep_combine_args, stream=None) -> int:

@@ -299,6 +299,51 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
                                                        s));
 }
 
+int ep_scatter_send(const ep_config *cfg, const ep_scatter_args *a, ep_stream_t stream)
+{
+    int rc = check_config(cfg);
+    if (rc != EP_OK)
+        return rc;
+    if (!a || !a->C || !a->expert_offsets || !a->src_info || !a->seg_offsets ||
+        !a->send_counts || !a->block_counter || !a->status)
+        return EP_ERR_INVALID_ARG;
+    if (!aligned16(a->C) || (reinterpret_cast<uintptr_t>(a->src_info) & 7u) ||
+        (reinterpret_cast<uintptr_t>(a->block_counter) & 3u))
+        return EP_ERR_INVALID_ARG;
+    if (a->max_rows < 1 || a->max_rows > INT32_MAX || cfg->N % 8 != 0)
+        return EP_ERR_INVALID_ARG;
+    const int R = cfg->n_ranks;
+    ep::ScatterParams p;
+    std::memset(&p, 0, sizeof p);
+    for (int r = 0; r < R; ++r) {
+        if (!a->recv_buf_ptrs[r] || !a->recv_count_ptrs[r] || !aligned16(a->recv_buf_ptrs[r]) ||
+            (reinterpret_cast<uintptr_t>(a->recv_count_ptrs[r]) & 7u))
+            return EP_ERR_INVALID_ARG;
+        p.recv_buf[r] = static_cast<uint8_t *>(a->recv_buf_ptrs[r]);
+        p.recv_count[r] = a->recv_count_ptrs[r];
+    }
+    const int num_sms = sm_count();
+    if (num_sms <= 0)
+        return EP_ERR_CUDA;
+    p.n_ranks = R;
+    p.my_rank = cfg->my_rank;
+    p.El = cfg->n_local_experts;
+    p.top_k = cfg->top_k;
+    p.N = cfg->N;
+    p.max_tokens = cfg->max_tokens_per_rank;
+    p.msg_bytes = cfg->msg_bytes;
+    p.max_rows = a->max_rows;
+    p.C = static_cast<const uint8_t *>(a->C);
+    p.expert_offsets = a->expert_offsets;
+    p.src_info = a->src_info;
+    p.seg_offsets = a->seg_offsets;
+    p.send_counts = a->send_counts;
+    p.block_counter = a->block_counter;
+    p.epoch = a->epoch;
+    p.status = a->status;
+    return cuda_status(ep::launch_scatter(p, num_sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int ep_combine_reduce(const ep_config *cfg, const ep_combine_args *a, ep_stream_t stream)
 {
     int rc = check_config(cfg);

@@ -40,6 +40,23 @@ struct SendParams {
     int trace_records;  // records per thread block
 };
 
+// The unfused send step (local C rows to the receive buffers, then signalling).
+struct ScatterParams {
+    int n_ranks, my_rank, El, top_k, N, max_tokens;
+    int64_t msg_bytes;
+    int64_t max_rows;
+    const uint8_t *C;
+    const int32_t *expert_offsets;
+    const int32_t *src_info;
+    const int32_t *seg_offsets;
+    const int32_t *send_counts;
+    uint8_t *recv_buf[EP_MAX_RANKS];
+    uint64_t *recv_count[EP_MAX_RANKS];
+    int32_t *block_counter;
+    uint64_t epoch;
+    uint32_t *status;
+};
+
 struct PlanParams {
     int n_ranks, my_rank, El, top_k, T;
     int64_t max_rows;
@@ -70,5 +87,6 @@ cudaError_t launch_gemm_send_fp8(const CUtensorMap &ta, const CUtensorMap &tb,
 cudaError_t launch_gemm_send_bf16_pair(const CUtensorMap &ta, const CUtensorMap &tb,
                                        const SendParams &p, int max_pairs, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, int num_sms, cudaStream_t s);
+cudaError_t launch_scatter(const ScatterParams &p, int num_sms, cudaStream_t s);
 
 }  // namespace ep

@@ -13,7 +13,8 @@ import numpy as np
 import torch
 
 from . import (EP_BF16, EP_FP8_1D2D, ep_combine_args, ep_combine_reduce, ep_config, ep_plan,
-               ep_plan_out, ep_plan_sizes, ep_send_args, grouped_gemm_combine_send, ptr)
+               ep_plan_out, ep_plan_sizes, ep_scatter_args, ep_scatter_send, ep_send_args,
+               grouped_gemm_combine_send, ptr)
 
 SENTINEL_BYTE = 0xFF  # received bf16 0xFFFF is a NaN: an unwritten slot cannot pass
 STATUS_PLAN, STATUS_SEND, STATUS_COMBINE = 0, 1, 2
@@ -40,6 +41,7 @@ class EpSystem:
                        for _ in range(R)]
         self.atomic_counter = [torch.zeros(El, dtype=torch.int32, device=dev) for _ in range(R)]
         self.rank_counter = [torch.zeros(R, dtype=torch.int32, device=dev) for _ in range(R)]
+        self.block_counter = [torch.zeros(1, dtype=torch.int32, device=dev) for _ in range(R)]
         self.status = torch.zeros(8, dtype=torch.int32, device=dev)
         self.topk = None
         self.plans: list[dict | None] = [None] * R
@@ -137,6 +139,34 @@ class EpSystem:
     def send(self, rank: int, epoch: int, stream=None, p3_control: int = 0, C=None):
         grouped_gemm_combine_send(self.cfg(rank), self.send_args(rank, epoch, p3_control, C),
                                   stream)
+
+    def local_C(self, rank: int):
+        """A [max_rows][N] bf16 buffer for the unfused path's local GEMM output."""
+        return torch.empty((self.ops[rank]["A"].shape[0], self.N), dtype=torch.bfloat16,
+                           device=self.device)
+
+    def send_unfused(self, rank: int, epoch: int, C, stream=None):
+        """The unfused comparator: the grouped GEMM with the sink disabled stores its
+        rows to the local C, then ep_scatter_send moves them and signals."""
+        grouped_gemm_combine_send(self.cfg(rank), self.send_args(rank, epoch, -1, C), stream)
+        ep_scatter_send(self.cfg(rank), self.scatter_args(rank, epoch, C), stream)
+
+    def scatter_args(self, rank: int, epoch: int, C) -> ep_scatter_args:
+        p = self.plans[rank]
+        a = ep_scatter_args()
+        a.C = ptr(C)
+        a.expert_offsets = ptr(p["expert_offsets"])
+        a.src_info = ptr(p["src_info"])
+        a.seg_offsets = ptr(p["seg_offsets"])
+        a.send_counts = ptr(p["send_counts"])
+        a.max_rows = min(int(C.shape[0]), int(p["src_info"].shape[0]))
+        for d in range(self.R):
+            a.recv_buf_ptrs[d] = ptr(self.recv[d])
+            a.recv_count_ptrs[d] = ptr(self.counts[d])
+        a.block_counter = ptr(self.block_counter[rank])
+        a.epoch = epoch
+        a.status = self.status.data_ptr() + 4 * STATUS_SEND
+        return a
 
     def send_traced(self, rank: int, epoch: int, records: int = 64, stream=None):
         """One send with per-tile timestamps; returns the decoded trace."""

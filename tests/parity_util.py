@@ -75,10 +75,14 @@ def build_system(w, routing, values, timeout_ns=0, send_warps=-1):
     return s
 
 
-def run_all(s, epoch: int):
-    """Every producer, then every destination's combine, on the current stream."""
+def run_all(s, epoch: int, unfused: bool = False):
+    """Every producer (the fused send, or the unfused GEMM into a local C followed by
+    ep_scatter_send), then every destination's combine, on the current stream."""
     for r in range(s.R):
-        s.send(r, epoch)
+        if unfused:
+            s.send_unfused(r, epoch, s.local_C(r))
+        else:
+            s.send(r, epoch)
     for d in range(s.R):
         s.combine(d, epoch)
 

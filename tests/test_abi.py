@@ -111,6 +111,33 @@ def test_unaligned_src_info_rejected(lib):
         ep.EP_ERR_INVALID_ARG
 
 
+def test_scatter_send_rejects_bad_arguments(lib):
+    """The unfused send step validates like the fused call, before any launch."""
+    cfg = _cfg()
+    assert lib.ep_scatter_send(ctypes.byref(cfg), ctypes.byref(ep.ep_scatter_args()),
+                               None) == ep.EP_ERR_INVALID_ARG
+    a = ep.ep_scatter_args()
+    a.C = 0x1000000
+    a.expert_offsets = a.seg_offsets = a.send_counts = a.status = 0x3000000
+    a.src_info = 0x3000008
+    a.block_counter = 0x6000000
+    a.max_rows = 8
+    for r in range(4):
+        a.recv_buf_ptrs[r] = 0x4000000 + r * 0x100000
+        a.recv_count_ptrs[r] = 0x5000000 + r * 0x100000
+    for field, bad in (("C", 0x1000008), ("src_info", 0x3000004), ("block_counter", 0x6000002)):
+        b = ep.ep_scatter_args.from_buffer_copy(a)
+        setattr(b, field, bad)
+        assert lib.ep_scatter_send(ctypes.byref(cfg), ctypes.byref(b), None) == \
+            ep.EP_ERR_INVALID_ARG, field
+    b = ep.ep_scatter_args.from_buffer_copy(a)
+    b.recv_buf_ptrs[2] = 0
+    assert lib.ep_scatter_send(ctypes.byref(cfg), ctypes.byref(b), None) == ep.EP_ERR_INVALID_ARG
+    bad_cfg = _cfg(n_ranks=9)
+    assert lib.ep_scatter_send(ctypes.byref(bad_cfg), ctypes.byref(a), None) == \
+        ep.EP_ERR_UNSUPPORTED
+
+
 def test_fp8_shape_rules(lib):
     """Blockwise fp8 needs whole 128-wide scale blocks along K and N."""
     a = ep.ep_send_args()

@@ -19,10 +19,10 @@ from synth import Routing, Workload, WORKLOADS, make_routing
 pytestmark = pytest.mark.gpu
 
 
-def _check_full(w, routing=None, values=None, epoch=3, send_warps=-1):
+def _check_full(w, routing=None, values=None, epoch=3, send_warps=-1, unfused=False):
     routing, values = (routing, values) if values is not None else make_inputs(w, routing)
     s = build_system(w, routing, values, send_warps=send_warps)
-    run_all(s, epoch)
+    run_all(s, epoch, unfused)
     torch.cuda.synchronize()
     st = s.status_words()
     assert (st == 0).all(), st
@@ -287,3 +287,31 @@ def test_fp8_identity_weights_bit_exact(T):
         np.testing.assert_array_equal(s.recv[d].cpu().numpy(), ref["recv"][d])
         np.testing.assert_array_equal(s.out[d].view(torch.int16).cpu().numpy().view(np.uint16),
                                       ref["out"][d])
+
+
+UNFUSED_CASES = [
+    ("tiny", WORKLOADS["tiny"]),
+    ("hot_pair_ragged", EDGE[0][1]),
+    ("eight_ranks_one_expert", EDGE[5][1]),
+    ("pair_shape", Workload("uf_pair", 4, 3, 2, 400, 320, 512, "bf16", "zipf", "softmax_sel", 66)),
+    ("fp8_small", EDGE[10][1]),
+]
+
+
+@pytest.mark.parametrize("name,w", UNFUSED_CASES, ids=[c[0] for c in UNFUSED_CASES])
+def test_unfused_send_parity(name, w):
+    """The unfused comparator (sink disabled: rows to a local C; then
+    ep_scatter_send) delivers the same rows, counts and flags as the fused call."""
+    routing, values = make_inputs(w)
+    if name == "hot_pair_ragged":
+        ids = np.tile(np.array([2, 3], np.int32), (w.n_ranks, w.tokens, 1))
+        routing = _fixed_routing(w, ids)
+    s, ref, routing, values = _check_full(w, routing, epoch=4, unfused=True)
+    # a second call re-arms the block counter and publishes the new epoch
+    run_all(s, 5, unfused=True)
+    torch.cuda.synchronize()
+    assert (s.status_words() == 0).all()
+    for d in range(w.n_ranks):
+        flags = s.counts[d].cpu().numpy().view(np.uint64)[w.n_local_experts * w.n_ranks:]
+        assert (flags == 5).all()
+        assert int(s.block_counter[d].item()) == 0
