@@ -68,6 +68,9 @@ def parse_args():
     ap.add_argument("--path", choices=["fused", "unfused"], default="fused",
                     help="unfused: the comparator without the sink (GEMM rows to a local C, "
                          "then ep_scatter_send); times the same step")
+    ap.add_argument("--signal-mode", choices=["rank_flag", "per_expert"], default="rank_flag",
+                    help="completion signalling: ep_ord_r rank flags (default) or per-expert "
+                         "count words with a per-token wait in the combine")
     ap.add_argument("--send-warps", type=int, default=-1, choices=[-1, 0, 4],
                     help="sink placement: -1 library choice, 0 inside the output warps, "
                          "4 dedicated send warps (bf16)")
@@ -296,7 +299,8 @@ def main():
     values = {r: make_rank_values(w, r, int(rows[r])) for r in ranks}
 
     s = EpSystem(w.n_ranks, w.n_local_experts, w.top_k, w.tokens, w.K, w.N, w.dtype,
-                 send_warps=args.send_warps)
+                 send_warps=args.send_warps,
+                 signal_mode=1 if args.signal_mode == "per_expert" else 0)
     s.set_routing(routing.topk_ids)
     for r in ranks:
         s.plan(r)
@@ -317,6 +321,22 @@ def main():
     stream = torch.cuda.current_stream()
     peer_idx = torch.tensor([w.n_local_experts * w.n_ranks + r for r in range(w.n_ranks)
                              if r != q], dtype=torch.int64, device="cuda")
+    # per-expert signalling: the peers' count words of rank q's buffer, (rk, e) ->
+    # e*R + rk, each holding the rows rank rk's expert e sends to q (from the routing)
+    peers = [rk for rk in range(w.n_ranks) if rk != q]
+    ids_q = routing.topk_ids[q].reshape(-1)
+    pe_idx = torch.tensor([e * w.n_ranks + rk for rk in peers for e in range(w.n_local_experts)],
+                          dtype=torch.int64, device="cuda")
+    pe_rows = torch.tensor([int((ids_q == rk * w.n_local_experts + e).sum()) for rk in peers
+                            for e in range(w.n_local_experts)], dtype=torch.int64, device="cuda")
+
+    def publish_peers(e: int):
+        """Stand-in for the other ranks finishing on their own GPUs."""
+        if args.signal_mode == "per_expert":
+            if pe_idx.numel():
+                s.counts[q].index_copy_(0, pe_idx, pe_rows + ((e & 0xFFFFFFFF) << 32))
+        elif peer_idx.numel():
+            s.counts[q].index_fill_(0, peer_idx, e)
     step_bytes = int(s.ops[q]["A"].numel() * s.ops[q]["A"].element_size()
                      + s.ops[q]["W"].numel() * s.ops[q]["W"].element_size())
     flush = torch.empty(512 * 2**20, dtype=torch.uint8, device="cuda") \
@@ -330,8 +350,7 @@ def main():
         epoch[0] += 1
         if flush is not None:
             flush.fill_(e & 0xFF)
-        if peer_idx.numel():
-            s.counts[q].index_fill_(0, peer_idx, e)
+        publish_peers(e)
         if evs is not None:
             evs[0].record(stream)
         if unfused:
@@ -376,7 +395,7 @@ def main():
         from moe_expert_gemm_gb300.system import summarize_trace
         e = epoch[0]
         epoch[0] += 1
-        s.counts[q].index_fill_(0, peer_idx, e)
+        publish_peers(e)
         tr = s.send_traced(q, e, records=256)
         if not args.solo:
             s.combine(q, e, stream)
@@ -422,8 +441,7 @@ def main():
             stream.wait_event(h2d_done)
             if out_free[b] is not None:
                 stream.wait_event(out_free[b])
-            if peer_idx.numel():
-                s.counts[q].index_fill_(0, peer_idx, e)
+            publish_peers(e)
             a = s.send_args(q, e)
             a.A = ep.ptr(A_bufs[b])
             if fp8:
@@ -510,6 +528,7 @@ def main():
                    "top_k": w.top_k, "tokens_per_rank": w.tokens, "K": w.K, "N": w.N,
                    "operands": w.dtype, "my_rank": q, "rows": m_rows,
                    "send_warps": args.send_warps, "path": args.path,
+                   "signal_mode": args.signal_mode,
                    "l2": ("flushed with a 512 MB write before every step" if flush is not None
                           else f"per-step inputs {step_bytes / 1e6:.0f} MB > L2"),
                    "parallelism": "replicas: one logical rank per GPU" if world > 1

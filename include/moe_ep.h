@@ -57,6 +57,16 @@ typedef struct CUstream_st *ep_stream_t;
 #define EP_STATUS_ROUTING 0x8u  /* ep_plan: an expert id outside [0, n_ranks*n_local_experts) */
 #define EP_STATUS_INTERNAL 0x10u /* a CTA pair found inconsistent tensor-memory bases: no work done */
 
+/* completion signalling ("ep_signal_completion") */
+#define EP_SIGNAL_RANK_FLAG 0  /* ep_ord_r with has_rank_flag: plain count words, an
+                                  acquire-release election per destination, the elected
+                                  producer release-stores the rank flag; the consumer
+                                  acquires one flag per source rank */
+#define EP_SIGNAL_PER_EXPERT 1 /* the default mode: every expert's count word is its own
+                                  arrival signal, released once the expert's rows are
+                                  written; no election, no rank flag; the consumer
+                                  acquires, per token, the words of that token's experts */
+
 /* operand types */
 #define EP_BF16 0     /* bf16 A and W, fp32 accumulation, bf16 rows */
 #define EP_FP8_1D2D 1 /* e4m3 A (1x128 fp32 scales) and W (128x128 fp32 scales), bf16 rows */
@@ -82,6 +92,8 @@ typedef struct CUstream_st *ep_stream_t;
  *                        single CTAs; fp8 gives EP_ERR_UNSUPPORTED); -1 lets the
  *                        library choose (today: inside the output warps). Any other
  *                        value gives EP_ERR_INVALID_ARG.
+ *   signal_mode          EP_SIGNAL_RANK_FLAG or EP_SIGNAL_PER_EXPERT; producers and
+ *                        consumers of one exchange must use the same mode.
  */
 typedef struct {
     int32_t n_ranks;
@@ -95,6 +107,7 @@ typedef struct {
     int32_t msg_bytes;
     int32_t dtype;
     int32_t send_warps;
+    int32_t signal_mode;
 } ep_config;
 
 /* ------------------------------------------------------------------ plan */
@@ -160,13 +173,17 @@ int ep_plan(const ep_config *cfg, const int32_t *topk_ids, const ep_plan_out *ou
  *                    each: word e*n_ranks + rk holds the rows expert e of rank rk sent
  *                    ("P3PeerSendConfig" recv_count_layout); word E_l*n_ranks + rk is
  *                    rank rk's completion flag ("ep_signal_completion" rank_flag_offset,
- *                    the buffer tail).
+ *                    the buffer tail). With EP_SIGNAL_RANK_FLAG a count word holds the
+ *                    row count and the flag the epoch; with EP_SIGNAL_PER_EXPERT a
+ *                    count word holds (epoch mod 2^32) << 32 | rows and the flag words
+ *                    are not written.
  *   atomic_counter   [E_l] int32 tile-completion counters of my_rank's experts
  *   rank_completion_counter  [n_ranks] int32 election counters, one per destination
  *                    Both counter arrays must be zero before the first call; every
  *                    call that completes without a status bit leaves them at zero.
- *   epoch            value released into the rank flags; use a new value per call
- *                    (e.g. 1, 2, 3, ...) so a consumer can tell calls apart.
+ *   epoch            value released into the rank flags (or the count words' high
+ *                    half); use a new value per call (e.g. 1, 2, 3, ...) so a consumer
+ *                    can tell calls apart.
  *   p3_control       >= 0: the sink owns the output (no local C); < 0: the sink is
  *                    disabled and rows go to the local C instead, with no signalling
  *                    ("EpiloguePeerSink" p3_control: negative disables the sink).
@@ -308,8 +325,13 @@ int ep_scatter_send(const ep_config *cfg, const ep_scatter_args *args, ep_stream
  *   epoch       the flag value to wait for from every source rank
  *   timeout_ns  limit of the flag wait (0: 2 s); on expiry EP_STATUS_TIMEOUT is set
  *               and the affected outputs are left unwritten
- * Each thread block acquires every source rank's flag once (system scope) before
- * reading the rows, as the fused consumer of "ep_signal_completion" does.
+ *   topk_ids    EP_SIGNAL_PER_EXPERT only: this rank's routing, [num_tokens][top_k]
+ *               global expert ids (the table ep_plan reads, rank my_rank's part)
+ * EP_SIGNAL_RANK_FLAG: each thread block acquires every source rank's flag once
+ * (system scope) before reading the rows, as the fused consumer of
+ * "ep_signal_completion" does. EP_SIGNAL_PER_EXPERT: before reducing a token, the
+ * warp acquires the count words of that token's top_k experts, so tokens whose
+ * experts have all arrived are reduced even while other experts are still sending.
  */
 typedef struct {
     const uint8_t *recv_buf;
@@ -319,6 +341,7 @@ typedef struct {
     uint64_t epoch;
     int64_t timeout_ns;
     uint32_t *status;
+    const int32_t *topk_ids;
 } ep_combine_args;
 
 int ep_combine_reduce(const ep_config *cfg, const ep_combine_args *args, ep_stream_t stream);

@@ -25,6 +25,8 @@ EP_ERR_CUDA = -3
 EP_STATUS_BOUNDS = 0x1
 EP_STATUS_TIMEOUT = 0x2
 EP_STATUS_CAPACITY = 0x4
+EP_SIGNAL_RANK_FLAG = 0
+EP_SIGNAL_PER_EXPERT = 1
 EP_STATUS_ROUTING = 0x8
 EP_STATUS_INTERNAL = 0x10
 
@@ -37,7 +39,7 @@ _c_i32, _c_i64, _c_u64, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, c
 class ep_config(ctypes.Structure):
     _fields_ = [(n, _c_i32) for n in ("n_ranks", "my_rank", "n_local_experts", "top_k",
                                       "num_tokens", "max_tokens_per_rank", "K", "N",
-                                      "msg_bytes", "dtype", "send_warps")]
+                                      "msg_bytes", "dtype", "send_warps", "signal_mode")]
 
 
 class ep_plan_out(ctypes.Structure):
@@ -58,7 +60,8 @@ class ep_send_args(ctypes.Structure):
 
 class ep_combine_args(ctypes.Structure):
     _fields_ = [("recv_buf", _vp), ("recv_count", _vp), ("gates", _vp), ("out", _vp),
-                ("epoch", _c_u64), ("timeout_ns", _c_i64), ("status", _vp)]
+                ("epoch", _c_u64), ("timeout_ns", _c_i64), ("status", _vp),
+                ("topk_ids", _vp)]
 
 
 class ep_scatter_args(ctypes.Structure):

@@ -89,6 +89,8 @@ int check_config(const ep_config *c)
         return EP_ERR_INVALID_ARG;
     if (c->send_warps != -1 && c->send_warps != 0 && c->send_warps != 4)
         return EP_ERR_INVALID_ARG;
+    if (c->signal_mode != EP_SIGNAL_RANK_FLAG && c->signal_mode != EP_SIGNAL_PER_EXPERT)
+        return EP_ERR_INVALID_ARG;
     // every index the kernels form from (token, slot) stays in 32 bits
     if (static_cast<int64_t>(c->max_tokens_per_rank) * c->n_ranks * c->top_k >= INT32_MAX)
         return EP_ERR_UNSUPPORTED;
@@ -273,6 +275,7 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     p.rank_counter = a->rank_completion_counter;
     p.epoch = a->epoch;
     p.sink_enabled = sink ? 1 : 0;
+    p.signal_mode = cfg->signal_mode;
     p.C = static_cast<uint8_t *>(a->C);
     p.status = a->status;
     p.timeout_ns = a->timeout_ns > 0 ? static_cast<uint64_t>(a->timeout_ns) : kDefaultTimeoutNs;
@@ -341,6 +344,7 @@ int ep_scatter_send(const ep_config *cfg, const ep_scatter_args *a, ep_stream_t 
     p.block_counter = a->block_counter;
     p.epoch = a->epoch;
     p.status = a->status;
+    p.signal_mode = cfg->signal_mode;
     return cuda_status(ep::launch_scatter(p, num_sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -353,6 +357,8 @@ int ep_combine_reduce(const ep_config *cfg, const ep_combine_args *a, ep_stream_
         return EP_ERR_INVALID_ARG;
     if (cfg->num_tokens > 0 && (!a->gates || !a->out))
         return EP_ERR_INVALID_ARG;
+    if (cfg->signal_mode == EP_SIGNAL_PER_EXPERT && cfg->num_tokens > 0 && !a->topk_ids)
+        return EP_ERR_INVALID_ARG;  // the per-token wait needs the token's experts
     if (cfg->N % 8 != 0 || !aligned16(a->recv_buf) || (a->out && !aligned16(a->out)) ||
         (reinterpret_cast<uintptr_t>(a->recv_count) & 7u))
         return EP_ERR_INVALID_ARG;
@@ -373,6 +379,8 @@ int ep_combine_reduce(const ep_config *cfg, const ep_combine_args *a, ep_stream_
     p.epoch = a->epoch;
     p.timeout_ns = a->timeout_ns > 0 ? static_cast<uint64_t>(a->timeout_ns) : kDefaultTimeoutNs;
     p.status = a->status;
+    p.topk_ids = a->topk_ids;
+    p.signal_mode = cfg->signal_mode;
     return cuda_status(ep::launch_combine(p, num_sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -2,7 +2,9 @@
 //
 // "ep_signal_completion" (ep_ord_r): a fused consumer acquires one rank-completion
 // flag per source rank instead of one word per expert; the single system-scope
-// release of the elected producer carries all of that rank's rows and counts. The
+// release of the elected producer carries all of that rank's rows and counts. In
+// the per-expert mode the consumer instead acquires, per token, the count words of
+// that token's experts (combine_kernel_per_expert). The
 // sum itself, out[t] = sum_j g[t, j] * row(t, j), is the combine role the
 // "P3PeerSendConfig" description names (EPCombineKernel), whose receive layout is
 // (src_idx*top_k + src_topk)*msg_bytes + byte_off.
@@ -119,6 +121,145 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     }
 }
 
+// EP_SIGNAL_PER_EXPERT: wait for (acquire) the count word of global expert g in this
+// rank's count buffer, (epoch mod 2^32) << 32 | rows, which g's owner releases once
+// all of g's rows are written. Bounded; after one wait of the block has run out,
+// later waits give up at once instead of each waiting out the limit.
+__device__ __forceinline__ bool expert_arrived(const CombineParams &p, int g, volatile int *gave_up)
+{
+    const int rk = g / p.El, e = g - rk * p.El;
+    const uint64_t *w = p.recv_count + static_cast<int64_t>(e) * p.n_ranks + rk;
+    const uint32_t tag = static_cast<uint32_t>(p.epoch);
+    if (static_cast<uint32_t>(ld_acquire_sys_u64(w) >> 32) == tag)
+        return true;
+    if (*gave_up)
+        return false;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(100);
+        if (static_cast<uint32_t>(ld_acquire_sys_u64(w) >> 32) == tag)
+            return true;
+        if (*gave_up)
+            return false;
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+            atomicOr(p.status, EP_STATUS_TIMEOUT);
+            *gave_up = 1;
+            return false;
+        }
+    }
+}
+
+// EP_SIGNAL_PER_EXPERT: the warp's lanes acquire the count words of token t's
+// top_k experts (warp-collective); true when all arrived. A malformed expert id
+// counts as never arriving and raises EP_STATUS_ROUTING.
+__device__ __forceinline__ bool token_arrived(const CombineParams &p, int64_t t, int k, int lane,
+                                              volatile int *gave_up)
+{
+    const int n_experts = p.n_ranks * p.El;
+    bool ok = true;
+    for (int j = lane; j < k; j += 32) {
+        const int g = __ldg(p.topk_ids + t * k + j);
+        if (g < 0 || g >= n_experts) {
+            atomicOr(p.status, EP_STATUS_ROUTING);
+            ok = false;
+        } else {
+            ok = expert_arrived(p, g, gave_up) && ok;
+        }
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    __syncwarp();  // the acquiring lanes' reads precede every lane's row loads
+    return ok;
+}
+
+// EP_SIGNAL_PER_EXPERT consumer: every warp takes a contiguous range of (token,
+// 256-column unit) work items and, whenever its range enters a new token, acquires
+// that token's experts; then it reduces the token's units U = max(1, kLoads / K) at
+// a time, all U*K row loads issued before accumulating. A token whose experts have
+// all arrived is reduced whatever the other experts are doing; one whose expert
+// never arrives is left unwritten (EP_STATUS_TIMEOUT). K = 0: top_k known at run
+// time only.
+template <int K>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel_per_expert(const CombineParams p)
+{
+    __shared__ int s_gave_up;
+    if (threadIdx.x == 0)
+        s_gave_up = 0;
+    __syncthreads();
+    volatile int *gave_up = &s_gave_up;
+    constexpr int U = K == 0 ? 1 : (K >= kLoads ? 1 : kLoads / K);
+    const int k = K == 0 ? p.top_k : K;
+    const int lane = threadIdx.x & 31;
+    const int64_t vec_per_row = p.N / 8;
+    const int64_t units_per_row = (vec_per_row + 31) / 32;
+    const int64_t units = static_cast<int64_t>(p.T) * units_per_row;
+    const int64_t n_warps = static_cast<int64_t>(gridDim.x) * (kCombineThreads / 32);
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * (kCombineThreads / 32) + (threadIdx.x >> 5);
+    const int64_t per = (units + n_warps - 1) / n_warps;
+    const int64_t u_end = (gw + 1) * per < units ? (gw + 1) * per : units;
+    for (int64_t u = gw * per; u < u_end;) {
+        const int64_t t = u / units_per_row;
+        const int64_t stop = (t + 1) * units_per_row < u_end ? (t + 1) * units_per_row : u_end;
+        if (token_arrived(p, t, k, lane, gave_up)) {
+            const uint8_t *rows_t = p.recv_buf + t * k * p.msg_bytes;
+            const float *g = p.gates + t * k;
+            for (int64_t u0 = u; u0 < stop; u0 += U) {
+                int64_t vv[U];
+                bool live[U];
+#pragma unroll
+                for (int uu = 0; uu < U; ++uu) {
+                    vv[uu] = (u0 + uu - t * units_per_row) * 32 + lane;
+                    live[uu] = u0 + uu < stop && vv[uu] < vec_per_row;
+                }
+                if constexpr (K > 0) {
+                    uint4 r[U][K];
+#pragma unroll
+                    for (int uu = 0; uu < U; ++uu)
+#pragma unroll
+                        for (int jj = 0; jj < K; ++jj)
+                            if (live[uu])
+                                r[uu][jj] = __ldcs(reinterpret_cast<const uint4 *>(
+                                    rows_t + jj * p.msg_bytes + vv[uu] * 16));
+#pragma unroll
+                    for (int uu = 0; uu < U; ++uu) {
+                        if (!live[uu])
+                            continue;
+                        float acc[8];
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            acc[c] = 0.f;
+#pragma unroll
+                        for (int jj = 0; jj < K; ++jj)
+                            accumulate_row(acc, __ldg(g + jj), r[uu][jj]);
+                        store_out(p, t, vv[uu], acc);
+                    }
+                } else {
+                    // run-time top_k: one unit, rows streamed kLoads at a time
+                    if (!live[0])
+                        continue;
+                    float acc[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        acc[c] = 0.f;
+                    for (int j = 0; j < k; j += kLoads) {
+                        uint4 rr[kLoads];
+#pragma unroll
+                        for (int jj = 0; jj < kLoads; ++jj)
+                            if (j + jj < k)
+                                rr[jj] = __ldcs(reinterpret_cast<const uint4 *>(
+                                    rows_t + (j + jj) * p.msg_bytes + vv[0] * 16));
+#pragma unroll
+                        for (int jj = 0; jj < kLoads; ++jj)
+                            if (j + jj < k)
+                                accumulate_row(acc, __ldg(g + j + jj), rr[jj]);
+                    }
+                    store_out(p, t, vv[0], acc);
+                }
+            }
+        }
+        u = stop;
+    }
+}
+
 // any other top_k: one unit at a time, its rows streamed kLoads at a time
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel_any(const CombineParams p)
 {
@@ -182,8 +323,32 @@ static cudaError_t launch_k(const CombineParams &p, int num_sms, cudaStream_t s)
     return cudaGetLastError();
 }
 
+template <int K>
+static cudaError_t launch_per_expert(const CombineParams &p, int num_sms, cudaStream_t s)
+{
+    constexpr int U = K == 0 ? 1 : (K >= kLoads ? 1 : kLoads / K);
+    const int64_t units = static_cast<int64_t>(p.T) * ((p.N / 8 + 31) / 32);
+    const int b = blocks_for(combine_kernel_per_expert<K>, num_sms, (units + 8 * U - 1) / (8 * U));
+    combine_kernel_per_expert<K><<<b, kCombineThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const CombineParams &p, int num_sms, cudaStream_t s)
 {
+    if (p.signal_mode == EP_SIGNAL_PER_EXPERT) {
+        switch (p.top_k) {
+        case 1:
+            return launch_per_expert<1>(p, num_sms, s);
+        case 2:
+            return launch_per_expert<2>(p, num_sms, s);
+        case 4:
+            return launch_per_expert<4>(p, num_sms, s);
+        case 8:
+            return launch_per_expert<8>(p, num_sms, s);
+        default:
+            return launch_per_expert<0>(p, num_sms, s);
+        }
+    }
     switch (p.top_k) {
     case 1:
         return launch_k<1>(p, num_sms, s);

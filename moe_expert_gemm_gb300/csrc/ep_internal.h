@@ -31,6 +31,7 @@ struct SendParams {
     int32_t *rank_counter;
     uint64_t epoch;
     int sink_enabled;  // p3_control >= 0
+    int signal_mode;   // EP_SIGNAL_RANK_FLAG or EP_SIGNAL_PER_EXPERT
     uint8_t *C;        // local output when the sink is disabled
     uint32_t *status;
     uint64_t timeout_ns;
@@ -55,6 +56,7 @@ struct ScatterParams {
     int32_t *block_counter;
     uint64_t epoch;
     uint32_t *status;
+    int signal_mode;
 };
 
 struct PlanParams {
@@ -75,6 +77,8 @@ struct CombineParams {
     uint64_t epoch;
     uint64_t timeout_ns;
     uint32_t *status;
+    const int32_t *topk_ids;  // EP_SIGNAL_PER_EXPERT: [T][top_k] global expert ids
+    int signal_mode;
 };
 
 // Kernel launchers; each returns the launch's cudaError_t.

@@ -5,8 +5,9 @@
 // every row m < m_total goes to the receive buffer of the rank that owns its
 // token, at (src_idx*top_k + src_topk)*msg_bytes ("P3PeerSendConfig"), and the
 // rank is signalled as "ep_signal_completion" does: count words, then the rank
-// flag. One launch sends every local expert, so instead of an election per
-// expert the last thread block to finish publishes all count words and the flags.
+// flag (or, per expert, epoch-tagged count words). One launch sends every local
+// expert, so instead of an election per expert the last thread block to finish
+// publishes all count words and the flags.
 //
 // Memory-bound copy: one warp per row at a time, 16-byte loads and stores, each
 // row's bytes contiguous on both sides; grid = a few blocks per SM.
@@ -79,6 +80,23 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterP
     if (!s_last)
         return;
     const int R = p.n_ranks;
+    if (p.signal_mode == EP_SIGNAL_PER_EXPERT) {
+        // every count word is its expert's arrival signal, tagged with the epoch and
+        // released by a system-scope fence of the thread that stores it (after the
+        // barrier that orders it behind the acquire above); no rank flag
+        const uint64_t tag = (p.epoch & 0xFFFFFFFFull) << 32;
+        if (threadIdx.x < p.El * R)
+            fence_acq_rel_sys();
+        for (int i = threadIdx.x; i < p.El * R; i += blockDim.x) {
+            const int e = i / R, dst = i % R;
+            st_relaxed_sys_u64(p.recv_count[dst] + static_cast<int64_t>(e) * R + p.my_rank,
+                               tag | static_cast<uint32_t>(__ldg(p.send_counts + e * R + dst)));
+        }
+        __syncthreads();
+        if (threadIdx.x == 0)
+            *reinterpret_cast<volatile int *>(p.block_counter) = 0;
+        return;
+    }
     for (int i = threadIdx.x; i < p.El * R; i += blockDim.x) {
         const int e = i / R, dst = i % R;
         volatile uint64_t *w = p.recv_count[dst] + static_cast<int64_t>(e) * R + p.my_rank;

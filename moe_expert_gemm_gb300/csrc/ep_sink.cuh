@@ -69,6 +69,25 @@ __device__ __forceinline__ void store_counts(const SendParams &p, const SinkShar
     }
 }
 
+// EP_SIGNAL_PER_EXPERT: the count word is the expert's arrival signal, tagged with
+// the call's epoch ((epoch mod 2^32) << 32 | rows) and stored after the caller's
+// system-scope fence (a release by the PTX release pattern); no election, no flag.
+__device__ __forceinline__ void store_tagged_counts(const SendParams &p, const SinkShared *sh,
+                                                    int e)
+{
+    const int R = p.n_ranks;
+    const bool cached = p.El * R <= kCountCache;
+    const uint64_t tag = (p.epoch & 0xFFFFFFFFull) << 32;
+#pragma unroll
+    for (int dst = 0; dst < EP_MAX_RANKS; ++dst) {
+        if (dst < R) {
+            const int c = cached ? sh->counts[e * R + dst] : __ldg(p.send_counts + e * R + dst);
+            st_relaxed_sys_u64(sh->cnt[dst] + static_cast<int64_t>(e) * R + p.my_rank,
+                               tag | static_cast<uint32_t>(c));
+        }
+    }
+}
+
 static __device__ __noinline__ void elect_and_publish(const SendParams &p, const SinkShared *sh)
 {
     const int R = p.n_ranks;
@@ -248,19 +267,26 @@ static __device__ void completion_loop(const SendParams &p, SinkShared *sh)
     volatile int *done_p = &sh->q_done;
     volatile int *abort_flag = &sh->abort_flag;
     uint64_t *trace = trace_block(p);
+    const bool per_expert = p.signal_mode == EP_SIGNAL_PER_EXPERT;
     if (blockIdx.x == 0) {
         bool any_empty = false;
         for (int e = 0; e < p.El; ++e) {
             if (sh->eoff[e + 1] == sh->eoff[e]) {
-                store_counts(p, sh, e);
+                if (!per_expert)
+                    store_counts(p, sh, e);
                 any_empty = true;
             }
         }
         if (any_empty) {
             fence_acq_rel_sys();
-            for (int e = 0; e < p.El; ++e)
-                if (sh->eoff[e + 1] == sh->eoff[e])
-                    elect_and_publish(p, sh);
+            for (int e = 0; e < p.El; ++e) {
+                if (sh->eoff[e + 1] == sh->eoff[e]) {
+                    if (per_expert)
+                        store_tagged_counts(p, sh, e);
+                    else
+                        elect_and_publish(p, sh);
+                }
+            }
         }
     }
     int head = 0;
@@ -285,16 +311,20 @@ static __device__ void completion_loop(const SendParams &p, SinkShared *sh)
                 any |= last[j];
             }
             if (any) {
-                for (int j = 0; j < n; ++j)
-                    if (last[j])
-                        store_counts(p, sh, ent[j].x);
-                // acquire the experts' other tiles; release their rows and counts
+                if (!per_expert)
+                    for (int j = 0; j < n; ++j)
+                        if (last[j])
+                            store_counts(p, sh, ent[j].x);
+                // acquire the experts' other tiles; release their rows (and counts)
                 fence_acq_rel_sys();
             }
             for (int j = 0; j < n; ++j) {
                 if (last[j]) {
                     *reinterpret_cast<volatile int *>(&p.atomic_counter[ent[j].x]) = 0;
-                    elect_and_publish(p, sh);
+                    if (per_expert)
+                        store_tagged_counts(p, sh, ent[j].x);
+                    else
+                        elect_and_publish(p, sh);
                 }
                 if (trace && ent[j].y >= 0) {
                     uint64_t *rec = trace + 2 + 4 * ent[j].y;

@@ -23,7 +23,7 @@ STATUS_PLAN, STATUS_SEND, STATUS_COMBINE = 0, 1, 2
 class EpSystem:
     def __init__(self, n_ranks: int, n_local_experts: int, top_k: int, tokens: int, K: int,
                  N: int, dtype: str = "bf16", device="cuda", max_tokens: int | None = None,
-                 timeout_ns: int = 0, send_warps: int = -1):
+                 timeout_ns: int = 0, send_warps: int = -1, signal_mode: int = 0):
         self.R, self.El, self.k, self.T, self.K, self.N = (n_ranks, n_local_experts, top_k,
                                                            tokens, K, N)
         self.dtype = dtype
@@ -33,6 +33,7 @@ class EpSystem:
         self.msg_bytes = 2 * N
         self.timeout_ns = timeout_ns
         self.send_warps = send_warps
+        self.signal_mode = signal_mode  # EP_SIGNAL_RANK_FLAG or EP_SIGNAL_PER_EXPERT
         dev = self.device
         R, El = self.R, self.El
         self.recv = [torch.full((self.max_tokens * top_k * self.msg_bytes,), SENTINEL_BYTE,
@@ -52,7 +53,7 @@ class EpSystem:
     # ------------------------------------------------------------- set-up
     def cfg(self, rank: int) -> ep_config:
         return ep_config(self.R, rank, self.El, self.k, self.T, self.max_tokens, self.K, self.N,
-                         self.msg_bytes, self.dt_code, self.send_warps)
+                         self.msg_bytes, self.dt_code, self.send_warps, self.signal_mode)
 
     def reset_buffers(self):
         for b in self.recv:
@@ -185,7 +186,8 @@ class EpSystem:
         o = self.out[rank] if out is None else out
         return ep_combine_args(ptr(self.recv[rank]), ptr(self.counts[rank]), ptr(g), ptr(o),
                                epoch, self.timeout_ns,
-                               self.status.data_ptr() + 4 * STATUS_COMBINE)
+                               self.status.data_ptr() + 4 * STATUS_COMBINE,
+                               ptr(self.topk[rank]) if self.topk is not None else 0)
 
     def combine(self, rank: int, epoch: int, stream=None, gates=None, out=None):
         ep_combine_reduce(self.cfg(rank), self.combine_args(rank, epoch, gates, out), stream)

@@ -235,6 +235,24 @@ def signal(n_ranks: int, n_local_experts: int, rank: int, send_counts, epoch: in
     return log[:n].copy()
 
 
+def signal_per_expert(n_ranks: int, n_local_experts: int, rank: int, send_counts, epoch: int,
+                      recv_counts: list) -> np.ndarray:
+    """The default ("not ep_ord_r") mode of "ep_signal_completion": every expert's
+    count word is its own arrival signal, so it must tell this call from the last
+    one: word e*R + rank of every destination's count buffer becomes
+    (epoch mod 2^32) << 32 | rows; the rank-flag words are not written and there
+    is no election. Returns the event log [El*R, 4] = (0, expert, dst, 0)."""
+    R, El = n_ranks, n_local_experts
+    sc = np.asarray(send_counts, dtype=np.int64).reshape(El, R)
+    tag = (int(epoch) & 0xFFFFFFFF) << 32
+    log = []
+    for e in range(El):
+        for dst in range(R):
+            recv_counts[dst][e * R + rank] = np.uint64(tag | int(sc[e, dst]))
+            log.append((0, e, dst, 0))
+    return np.array(log, np.int32).reshape(-1, 4)
+
+
 # ------------------------------------------------------------------ combine
 
 def combine(recv_buf, gates, top_k: int, N: int, msg_bytes: int, tokens=None,

@@ -12,7 +12,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import (BF16, FP8_1D2D, Plan, combine, combine_exact, default_threads, expert_rows, plan,
-               scatter, signal)
+               scatter, signal, signal_per_expert)
 
 SENTINEL_BYTE = 0xFF  # bf16 0xFFFF is a NaN: an unwritten slot cannot pass a value check
 SENTINEL_WORD = np.uint64(0xFFFFFFFFFFFFFFFF)
@@ -22,7 +22,8 @@ def _dtype_code(dtype: str) -> int:
     return {"bf16": BF16, "fp8_1d2d": FP8_1D2D}[dtype]
 
 
-def full_pipeline(w, routing, values: list, epoch: int = 1, threads: int | None = None) -> dict:
+def full_pipeline(w, routing, values: list, epoch: int = 1, threads: int | None = None,
+                  per_expert: bool = False) -> dict:
     """Run every producer rank, then every destination's combine.
 
     ``values[r]`` is the operand dict of rank r (``synth.make_rank_values``).
@@ -30,7 +31,8 @@ def full_pipeline(w, routing, values: list, epoch: int = 1, threads: int | None 
     election counters per producer, signalling logs per producer, slot hit counts
     per destination, the combined outputs per destination (bf16 bits) and, as
     ``out_exact`` / ``rows_exact``, the exact combine of the exact rows (float64,
-    no rounding anywhere) per destination."""
+    no rounding anywhere) per destination. ``per_expert`` selects the default
+    signalling mode (epoch-tagged count words, no rank flags) instead of ep_ord_r."""
     R, El, k, T, K, N = w.n_ranks, w.n_local_experts, w.top_k, w.tokens, w.K, w.N
     msg = w.msg_bytes
     dt = _dtype_code(w.dtype)
@@ -55,7 +57,10 @@ def full_pipeline(w, routing, values: list, epoch: int = 1, threads: int | None 
         hits, b = scatter(Y, rows, pl, R, k, N, msg, T, recv, hits)
         bad += b
         ctr = np.zeros(R, np.int32)
-        logs.append(signal(R, El, r, pl.send_counts, epoch, counts, ctr))
+        if per_expert:
+            logs.append(signal_per_expert(R, El, r, pl.send_counts, epoch, counts))
+        else:
+            logs.append(signal(R, El, r, pl.send_counts, epoch, counts, ctr))
         counters.append(ctr)
         plans.append(pl)
         ys.append(Y)

@@ -62,10 +62,10 @@ def make_inputs(w, routing=None):
     return routing, values
 
 
-def build_system(w, routing, values, timeout_ns=0, send_warps=-1):
+def build_system(w, routing, values, timeout_ns=0, send_warps=-1, signal_mode=0):
     from moe_expert_gemm_gb300.system import EpSystem
     s = EpSystem(w.n_ranks, w.n_local_experts, w.top_k, w.tokens, w.K, w.N, w.dtype,
-                 timeout_ns=timeout_ns, send_warps=send_warps)
+                 timeout_ns=timeout_ns, send_warps=send_warps, signal_mode=signal_mode)
     s.set_routing(routing.topk_ids)
     for r in range(w.n_ranks):
         s.plan(r)

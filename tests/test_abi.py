@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(lib):
 def _cfg(**kw):
     base = dict(n_ranks=4, my_rank=0, n_local_experts=2, top_k=2, num_tokens=64,
                 max_tokens_per_rank=64, K=256, N=128, msg_bytes=256, dtype=ep.EP_BF16,
-                send_warps=-1)
+                send_warps=-1, signal_mode=0)
     base.update(kw)
     return ep.ep_config(**base)
 
@@ -58,6 +58,7 @@ def test_plan_sizes(lib):
     (dict(n_local_experts=300, top_k=2), ep.EP_ERR_UNSUPPORTED),
     (dict(dtype=7), ep.EP_ERR_INVALID_ARG),
     (dict(send_warps=3), ep.EP_ERR_INVALID_ARG),
+    (dict(signal_mode=2), ep.EP_ERR_INVALID_ARG),
 ])
 def test_bad_config_rejected_before_launch(lib, kw, code):
     cfg = _cfg(**kw)
@@ -152,6 +153,14 @@ def test_fp8_has_no_dedicated_send_warps(lib):
     cfg = _cfg(dtype=ep.EP_FP8_1D2D, send_warps=4)
     assert lib.grouped_gemm_combine_send(ctypes.byref(cfg), ctypes.byref(ep.ep_send_args()),
                                          None) == ep.EP_ERR_UNSUPPORTED
+
+
+def test_per_expert_combine_needs_the_routing(lib):
+    """In the per-expert mode the combine waits per token for the token's experts."""
+    cfg = _cfg(signal_mode=ep.EP_SIGNAL_PER_EXPERT)
+    a = ep.ep_combine_args(0x1000000, 0x2000000, 0x3000000, 0x4000000, 1, 0, 0x5000000, 0)
+    assert lib.ep_combine_reduce(ctypes.byref(cfg), ctypes.byref(a), None) == \
+        ep.EP_ERR_INVALID_ARG
 
 
 def test_strerror(lib):

@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import moe_expert_gemm_gb300 as ep
 import oracle
 from oracle.pipeline import full_pipeline
 from parity_util import (TOL, assert_plan_equal, build_system, combine_rel_err, make_inputs,
@@ -19,14 +20,15 @@ from synth import Routing, Workload, WORKLOADS, make_routing
 pytestmark = pytest.mark.gpu
 
 
-def _check_full(w, routing=None, values=None, epoch=3, send_warps=-1, unfused=False):
+def _check_full(w, routing=None, values=None, epoch=3, send_warps=-1, unfused=False,
+                per_expert=False):
     routing, values = (routing, values) if values is not None else make_inputs(w, routing)
-    s = build_system(w, routing, values, send_warps=send_warps)
+    s = build_system(w, routing, values, send_warps=send_warps, signal_mode=int(per_expert))
     run_all(s, epoch, unfused)
     torch.cuda.synchronize()
     st = s.status_words()
     assert (st == 0).all(), st
-    ref = full_pipeline(w, routing, values, epoch=epoch)
+    ref = full_pipeline(w, routing, values, epoch=epoch, per_expert=per_expert)
     tol = TOL[w.dtype]
     for r in range(w.n_ranks):
         assert_plan_equal(s.plan_host(r), ref["plans"][r])
@@ -315,3 +317,57 @@ def test_unfused_send_parity(name, w):
         flags = s.counts[d].cpu().numpy().view(np.uint64)[w.n_local_experts * w.n_ranks:]
         assert (flags == 5).all()
         assert int(s.block_counter[d].item()) == 0
+
+
+PER_EXPERT_CASES = [
+    ("tiny", WORKLOADS["tiny"], False),
+    ("empty_experts", EDGE[7][1], False),
+    ("eight_ranks_one_expert", EDGE[5][1], False),
+    ("topk3", EDGE[9][1], False),
+    ("pair_shape", Workload("pe_pair", 4, 3, 2, 400, 320, 512, "bf16", "zipf", "softmax_sel", 67),
+     False),
+    ("fp8_small", EDGE[10][1], False),
+    ("tiny_unfused", WORKLOADS["tiny"], True),
+]
+
+
+@pytest.mark.parametrize("name,w,unfused", PER_EXPERT_CASES, ids=[c[0] for c in PER_EXPERT_CASES])
+def test_per_expert_signalling_parity(name, w, unfused):
+    """EP_SIGNAL_PER_EXPERT (the pages' default mode): every expert's count word is an
+    epoch-tagged arrival signal, no rank flag is written, and the combine waits per
+    token for that token's experts. Same rows and outputs; count words as the oracle's
+    per-expert signalling writes them (flag words untouched)."""
+    routing = None
+    if name == "empty_experts":
+        rng = np.random.default_rng(9)
+        choices = np.array([0, 5, 6, 13], np.int32)
+        ids = np.stack([np.stack([rng.choice(choices, 2, replace=False) for _ in range(w.tokens)])
+                        for _ in range(w.n_ranks)])
+        routing = _fixed_routing(w, ids)
+    _check_full(w, routing, epoch=2**32 + 9, unfused=unfused, per_expert=True)
+
+
+def test_per_expert_tokens_of_finished_ranks_are_combined_while_one_rank_is_missing():
+    """With per-expert signals a token is reduced once its own experts have arrived:
+    when rank 3 never sends, exactly the tokens routed to one of rank 3's experts
+    time out (left unwritten, EP_STATUS_TIMEOUT); every other token is combined."""
+    w = WORKLOADS["tiny"]
+    routing, values = make_inputs(w)
+    s = build_system(w, routing, values, timeout_ns=30_000_000, signal_mode=1)
+    for r in range(w.n_ranks):
+        if r != 3:
+            s.send(r, epoch=1)
+    for d in range(w.n_ranks):
+        s.out[d].fill_(0)
+        s.combine(d, epoch=1)
+    torch.cuda.synchronize()
+    assert s.status_words()[2] & ep.EP_STATUS_TIMEOUT
+    ref = full_pipeline(w, routing, values, epoch=1, per_expert=True)
+    missing = routing.topk_ids // w.n_local_experts == 3
+    for d in range(w.n_ranks):
+        out = s.out[d].view(torch.int16).cpu().numpy().view(np.uint16)
+        waits = missing[d].any(axis=1)
+        assert waits.any() and (~waits).any()
+        assert (out[waits] == 0).all()
+        assert combine_rel_err(out[~waits], ref["out_exact"][d][~waits],
+                               ref["rows_exact"][d][~waits], routing.gates[d][~waits]) <= TOL["bf16"]

@@ -341,6 +341,30 @@ def test_signal_counts_and_flag_order():
             assert res["counts"][d][El * R + q] == 5
 
 
+def test_per_expert_signal_words_decode_to_the_plan_counts():
+    """Default mode: the high half of every count word is the call's epoch, the low
+    half the row count the brute-force-pinned plan gives; the flag words stay
+    untouched, and a later call re-tags every word."""
+    w = WORKLOADS["tiny"]
+    r = make_routing(w)
+    R, El = w.n_ranks, w.n_local_experts
+    bufs = [np.full(El * R + R, np.uint64(0xFFFFFFFFFFFFFFFF), np.uint64) for _ in range(R)]
+    for epoch in (7, 2**32 + 3):
+        for q in range(R):
+            pl = oracle.plan(R, El, w.top_k, r.topk_ids, q)
+            log = oracle.signal_per_expert(R, El, q, pl.send_counts, epoch, bufs)
+            assert len(log) == El * R and (log[:, 0] == 0).all()
+        for d in range(R):
+            words = bufs[d][:El * R].reshape(El, R)
+            assert ((words >> np.uint64(32)) == np.uint64(epoch & 0xFFFFFFFF)).all()
+            for q in range(R):
+                keys = _brute_plan(r.topk_ids, R, El, q)
+                for e in range(El):
+                    n = sum(1 for key in keys if key[0] == e and key[1] == d)
+                    assert int(words[e, q] & np.uint64(0xFFFFFFFF)) == n
+            assert (bufs[d][El * R:] == np.uint64(0xFFFFFFFFFFFFFFFF)).all()
+
+
 def test_signal_flag_never_before_last_expert():
     """With a counter already at El-2 for every destination, the first expert
     signalled must not publish the flag; the second must."""
