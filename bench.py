@@ -218,6 +218,33 @@ def cpu_sample(w, routing, values, dst: int, target_s: float, plans: dict):
     return n / dt, oracle.default_threads(), desc, n, dt
 
 
+# ----------------------------------------------------------- multi-process host logic
+# N > 1 runs N independent replicas (one logical rank per GPU, no data-path
+# collective): each process plays logical rank (rank mod n_ranks), the timed
+# region is bracketed by barriers, the step time is the maximum over processes
+# and the reported value is the whole job's tokens over that time.
+
+def replica_rank(rank: int, n_ranks: int) -> int:
+    """The logical rank a process plays."""
+    return rank % n_ranks
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The maximum of x over all processes (x itself when there is one)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_replica: int, step_ms: float) -> float:
+    """Whole-job throughput: every replica's tokens over the slowest replica's step."""
+    return world * tokens_per_replica / (step_ms / 1e3)
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -292,7 +319,7 @@ def main():
     if args.tokens:
         import dataclasses
         w = dataclasses.replace(w, tokens=args.tokens, name=f"{w.name}@T{args.tokens}")
-    q = rank % w.n_ranks  # the logical rank this process plays
+    q = replica_rank(rank, w.n_ranks)  # the logical rank this process plays
     routing = make_routing(w)
     rows = rows_per_rank(w, routing.topk_ids)
     ranks = [q] if args.solo else list(range(w.n_ranks))
@@ -481,16 +508,12 @@ def main():
         if not torch.equal(last.view(torch.int16), s.out[q].cpu().view(torch.int16)):
             raise SystemExit("end-to-end output differs from the device-timed output")
         if world > 1:
-            t = torch.tensor([e2e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e["value"] = world * w.tokens / (float(t.item()) / 1e3)
+            e2e["value"] = job_tokens_per_s(world, w.tokens,
+                                            max_over_ranks(e2e_ms, world, "cuda"))
         if s.status_words().any():
             raise SystemExit(f"device status after e2e: {s.status_words()}")
 
-    if world > 1:
-        t = torch.tensor([step_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(step_ms, world, "cuda")
 
     peaks, peak_src = load_peaks()
     send_s = statistics.mean(send_ms) / 1e3
@@ -519,7 +542,7 @@ def main():
     roof["algorithmic_per_launch"] = {"flops": flops, "bytes": send_bytes}
 
     line = {
-        "metric": METRIC, "value": world * w.tokens / (step_ms / 1e3), "unit": UNIT,
+        "metric": METRIC, "value": job_tokens_per_s(world, w.tokens, step_ms), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "e4m3",

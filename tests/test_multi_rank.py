@@ -1,0 +1,71 @@
+"""The N > 1 host path of bench.py on CPU: two processes over gloo (no GPU).
+
+N GPUs run N independent replicas: each process plays logical rank
+(rank mod n_ranks), the step time is the maximum over processes, the value is
+the whole job's tokens over that time, and the reference arm runs (and prints)
+on rank 0 only."""
+
+import io
+import os
+import sys
+from contextlib import redirect_stdout
+
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _worker(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        got_rank, _, got_world = bench.dist_env()
+        step_ms = [2.0, 3.5][rank]  # rank 1 is the slower replica
+        slowest = bench.max_over_ranks(step_ms, world, "cpu")
+        dist.barrier()
+        # the reference arm under torchrun: only rank 0 does work and prints
+        out = io.StringIO()
+        if rank != 0:
+            with redirect_stdout(out):
+                bench.run_reference(argparse_ns(), rank, world)
+        q.put(dict(rank=rank, env=(got_rank, got_world), replica=bench.replica_rank(rank, 8),
+                   slowest=slowest,
+                   value=bench.job_tokens_per_s(world, 4096, slowest),
+                   ref_out=out.getvalue()))
+    finally:
+        dist.destroy_process_group()
+
+
+def argparse_ns():
+    import argparse
+    return argparse.Namespace(workload="tiny", steps=1, warmup=0)
+
+
+def test_two_replicas_over_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29600 + os.getpid() % 1000
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted((q.get(timeout=120) for _ in procs), key=lambda d: d["rank"])
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r["env"] for r in res] == [(0, 2), (1, 2)]
+    assert [r["replica"] for r in res] == [0, 1]
+    assert all(r["slowest"] == 3.5 for r in res)  # every rank sees the maximum
+    assert all(abs(r["value"] - 2 * 4096 / 3.5e-3) < 1e-6 for r in res)
+    assert res[1]["ref_out"] == ""  # rank 1 of the reference arm prints nothing
+
+
+def test_single_process_helpers():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(1.25, 1, "cpu") == 1.25
+    assert bench.replica_rank(9, 8) == 1
+    assert bench.job_tokens_per_s(1, 1000, 2.0) == 500_000.0
