@@ -65,9 +65,10 @@ def parse_args():
                     help="after timing, run one traced send and write its summary here")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override tokens per rank (profiling a smaller case of a workload)")
-    ap.add_argument("--path", choices=["fused", "unfused"], default="fused",
+    ap.add_argument("--path", choices=["fused", "unfused", "layer"], default="fused",
                     help="unfused: the comparator without the sink (GEMM rows to a local C, "
-                         "then ep_scatter_send); times the same step")
+                         "then ep_scatter_send); layer: a whole MoE layer (dispatch, up/gate "
+                         "GEMM, activation, the fused down-projection + send, combine; bf16)")
     ap.add_argument("--signal-mode", choices=["rank_flag", "per_expert"], default="rank_flag",
                     help="completion signalling: ep_ord_r rank flags (default) or per-expert "
                          "count words with a per-token wait in the combine")
@@ -306,7 +307,7 @@ def main():
 
     import moe_expert_gemm_gb300 as ep
     from moe_expert_gemm_gb300.system import EpSystem
-    from synth import WORKLOADS, make_rank_values, make_routing, rows_per_rank
+    from synth import WORKLOADS, make_layer_values, make_rank_values, make_routing, rows_per_rank
 
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -323,7 +324,11 @@ def main():
     routing = make_routing(w)
     rows = rows_per_rank(w, routing.topk_ids)
     ranks = [q] if args.solo else list(range(w.n_ranks))
-    values = {r: make_rank_values(w, r, int(rows[r])) for r in ranks}
+    layer = args.path == "layer"
+    if layer and (w.dtype != "bf16" or args.solo):
+        raise SystemExit("--path layer runs bf16 workloads with every rank staged")
+    values = {r: (make_layer_values(w, r) if layer else make_rank_values(w, r, int(rows[r])))
+              for r in ranks}
 
     s = EpSystem(w.n_ranks, w.n_local_experts, w.top_k, w.tokens, w.K, w.N, w.dtype,
                  send_warps=args.send_warps,
@@ -332,11 +337,17 @@ def main():
     for r in ranks:
         s.plan(r)
         v = values[r]
-        s.set_operands(r, v["A"], v["W"], v.get("a_scales"), v.get("w_scales"))
+        if layer:
+            s.set_layer_operands(r, v["X"], v["W1"], v["W2"])
+        else:
+            s.set_operands(r, v["A"], v["W"], v.get("a_scales"), v.get("w_scales"))
     s.set_gates(q, routing.gates[q])
     # peers' rows land in every receive buffer once (their producers are not timed)
     for r in ranks:
-        s.send(r, epoch=1)
+        if layer:
+            s.layer_forward(r, epoch=1)
+        else:
+            s.send(r, epoch=1)
     torch.cuda.synchronize()
     st = s.status_words()
     if st.any():
@@ -380,7 +391,10 @@ def main():
         publish_peers(e)
         if evs is not None:
             evs[0].record(stream)
-        if unfused:
+        if layer:
+            s.layer_forward(q, e, stream, events=None if evs is None
+                            else [evs[4], evs[5], evs[6], evs[7]])
+        elif unfused:
             s.send(q, e, stream, p3_control=-1, C=C_local)
             if evs is not None:
                 evs[3].record(stream)
@@ -402,7 +416,7 @@ def main():
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     time.sleep(0.5)  # let the sampler start before the timed region
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
     torch.cuda.synchronize()
     for i in range(args.steps):
         one_step(events[i])
@@ -413,6 +427,9 @@ def main():
     send_ms = [e[0].elapsed_time(e[1]) for e in events]
     comb_ms = [e[1].elapsed_time(e[2]) for e in events]
     gemm_ms = [e[0].elapsed_time(e[3]) for e in events] if unfused else None
+    if layer:  # dispatch, up/gate GEMM, activation, fused down-projection + send
+        stage_ms = [statistics.mean(e[a].elapsed_time(e[b]) for e in events)
+                    for a, b in ((0, 4), (4, 5), (5, 6), (6, 7))]
     step_ms = sum(a + b for a, b in zip(send_ms, comb_ms)) / args.steps
     st = s.status_words()
     if st.any():
@@ -437,7 +454,7 @@ def main():
     # outputs double-buffered, so step i+1's host->device copies overlap step i's kernels
     # and step i's read-back overlaps step i+1's.
     e2e = None
-    if not args.no_e2e and not args.solo and not unfused:
+    if not args.no_e2e and not args.solo and not unfused and not layer:
         ops = s.ops[q]
         A_bufs = [ops["A"], torch.empty_like(ops["A"])]
         fp8 = "a_scales" in ops
@@ -518,14 +535,21 @@ def main():
     peaks, peak_src = load_peaks()
     send_s = statistics.mean(send_ms) / 1e3
     comb_s = statistics.mean(comb_ms) / 1e3
-    # the dominant kernel: the fused GEMM + send, or (unfused) the GEMM into the local C
-    dom_s = statistics.mean(gemm_ms) / 1e3 if unfused else send_s
+    # the dominant kernel: the fused GEMM + send, (unfused) the GEMM into the local C, or
+    # (layer) the up/gate GEMM
+    if layer:
+        flops = 2.0 * m_rows * w.N * 2 * w.K
+        send_bytes = m_rows * w.N * 2 + plan_q["send_counts"].shape[0] * 2 * w.K * w.N * 2 \
+            + m_rows * 2 * w.K * 2
+        dom_s = stage_ms[1] / 1e3
+    else:
+        dom_s = statistics.mean(gemm_ms) / 1e3 if unfused else send_s
     tflops = flops / dom_s / 1e12
     peak_tf = float(peaks["bf16_tflops"]) * (2.0 if w.dtype == "fp8_1d2d" else 1.0)
     peak_bw = float(peaks["hbm_gbs"])
     t_tensor = flops / (peak_tf * 1e12)
     t_hbm = send_bytes / (peak_bw * 1e9)
-    traffic = None if unfused else measured_traffic(w.name, "grouped_gemm_combine_send")
+    traffic = None if unfused or layer else measured_traffic(w.name, "grouped_gemm_combine_send")
     if t_tensor >= t_hbm:
         roof = {"bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": tflops / peak_tf, "traffic": traffic}
@@ -534,7 +558,8 @@ def main():
         roof = {"bound": "hbm", "achieved": gbs, "peak": peak_bw, "unit": "GB/s",
                 "frac": gbs / peak_bw, "traffic": traffic}
     roof["kernel"] = ("grouped_gemm_combine_send with the sink disabled (rows to a local C)"
-                      if unfused else "grouped_gemm_combine_send")
+                      if unfused else "the up/gate grouped GEMM (K = H, N = 2I, rows to a "
+                      "local buffer)" if layer else "grouped_gemm_combine_send")
     roof["peak_source"] = (f"{peak_src}: " + ("bf16_tflops (burst)" if roof["bound"] == "tensor"
                                               else "hbm_gbs")
                            + (" x2 nominal fp8/bf16 ratio" if w.dtype == "fp8_1d2d"
@@ -557,21 +582,28 @@ def main():
                    "parallelism": "replicas: one logical rank per GPU" if world > 1
                    else "one logical rank"},
         "tflops": tflops,
-        "kernels_ms": ({"grouped_gemm_combine_send (local C)": statistics.mean(gemm_ms),
+        "kernels_ms": ({"ep_dispatch_gather": stage_ms[0],
+                        "up/gate grouped_gemm_combine_send (local buffer)": stage_ms[1],
+                        "ep_swiglu": stage_ms[2], "grouped_gemm_combine_send": stage_ms[3],
+                        "ep_combine_reduce": statistics.mean(comb_ms)} if layer else
+                       {"grouped_gemm_combine_send (local C)": statistics.mean(gemm_ms),
                         "ep_scatter_send": statistics.mean(send_ms) - statistics.mean(gemm_ms),
                         "ep_combine_reduce": statistics.mean(comb_ms)} if unfused else
                        {"grouped_gemm_combine_send": statistics.mean(send_ms),
                         "ep_combine_reduce": statistics.mean(comb_ms)}),
         "combine_gbs": comb_bytes / comb_s / 1e9,
         "roofline": roof,
-        "gpu_launches": (3 if unfused else 2) * args.steps,
+        "gpu_launches": (5 if layer else 3 if unfused else 2) * args.steps,
         "clocks": clk,
     }
     if e2e is not None:
         line["e2e"] = e2e
     if args.solo:
         line["config"]["solo"] = "profiling aid: fused send only, peers not staged"
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.solo:
+    if layer:
+        line["config"]["layer"] = {"hidden": w.N, "intermediate": w.K,
+                                   "metric": "tokens/s of the whole layer for one rank"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.solo and not layer:
         import oracle
         plans = {r: oracle.plan(w.n_ranks, w.n_local_experts, w.top_k, routing.topk_ids, r)
                  for r in range(w.n_ranks)}

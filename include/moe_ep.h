@@ -314,6 +314,60 @@ typedef struct {
 
 int ep_scatter_send(const ep_config *cfg, const ep_scatter_args *args, ep_stream_t stream);
 
+/* ------------------------------------------------------------- MoE layer */
+
+/*
+ * The steps before the down-projection, for running a whole MoE layer on this
+ * library: dispatch, the up/gate projection, the gated activation. The pages
+ * describe only the down-projection and its combine; they imply the dispatch
+ * through the plan's row order and src_info. The up/gate projection is
+ * grouped_gemm_combine_send itself with p3_control < 0 (rows to a local buffer),
+ * called with K = hidden size and N = 2 * intermediate size (msg_bytes = 2*N).
+ *
+ * ep_dispatch_gather -- every routed token row to the rank that owns its expert,
+ * in plan order.
+ *   x_ptrs          [n_ranks] source ranks' tokens, [max_tokens_per_rank][hidden]
+ *                   bf16 each (peer memory or, on one GPU, other allocations)
+ *   gather_idx, expert_offsets   the plan of my_rank (ep_plan)
+ *   max_rows        rows allocated for A_in
+ *   hidden          row length in elements, a multiple of 8
+ *   A_in            [max_rows][hidden] bf16 out: row m = x_rk[t] for the plan's
+ *                   row m = (rk, t, j)
+ *   status          EP_STATUS_BOUNDS for a gather index outside the token tables
+ *                   (that row skipped)
+ */
+typedef struct {
+    const void *x_ptrs[EP_MAX_RANKS];
+    const int32_t *gather_idx;
+    const int32_t *expert_offsets;
+    int64_t max_rows;
+    int32_t hidden;
+    void *A_in;
+    uint32_t *status;
+} ep_dispatch_args;
+
+int ep_dispatch_gather(const ep_config *cfg, const ep_dispatch_args *args, ep_stream_t stream);
+
+/*
+ * ep_swiglu -- the gated activation between the up/gate and down projections:
+ *   A[m][i] = bf16( SiLU(G[m][i]) * G[m][inter + i] ),  SiLU(x) = x / (1 + e^-x),
+ * in fp32 from the bf16 G, rounded to nearest even once, for m below the plan's
+ * row count.
+ *   G               [max_rows][2*inter] bf16: the up/gate GEMM's rows, gate half first
+ *   A               [max_rows][inter] bf16 out: the down-projection's A
+ *   expert_offsets  the plan of my_rank (row count at [E_l])
+ *   inter           a multiple of 8
+ */
+typedef struct {
+    const void *G;
+    void *A;
+    const int32_t *expert_offsets;
+    int64_t max_rows;
+    int32_t inter;
+} ep_swiglu_args;
+
+int ep_swiglu(const ep_config *cfg, const ep_swiglu_args *args, ep_stream_t stream);
+
 /* --------------------------------------------------------------- combine */
 
 /*

@@ -71,6 +71,16 @@ class ep_scatter_args(ctypes.Structure):
                 ("block_counter", _vp), ("epoch", _c_u64), ("status", _vp)]
 
 
+class ep_dispatch_args(ctypes.Structure):
+    _fields_ = [("x_ptrs", _vp * EP_MAX_RANKS), ("gather_idx", _vp), ("expert_offsets", _vp),
+                ("max_rows", _c_i64), ("hidden", _c_i32), ("A_in", _vp), ("status", _vp)]
+
+
+class ep_swiglu_args(ctypes.Structure):
+    _fields_ = [("G", _vp), ("A", _vp), ("expert_offsets", _vp), ("max_rows", _c_i64),
+                ("inter", _c_i32)]
+
+
 class EpError(RuntimeError):
     def __init__(self, code: int, where: str):
         super().__init__(f"{where}: {ep_strerror(code)} ({code})")
@@ -80,7 +90,8 @@ class EpError(RuntimeError):
 _lib = None
 
 EXPORTS = ("ep_plan_sizes", "ep_plan", "grouped_gemm_combine_send", "ep_combine_reduce",
-           "ep_strerror", "grouped_gemm_combine_send_noalloc", "ep_scatter_send")
+           "ep_strerror", "grouped_gemm_combine_send_noalloc", "ep_scatter_send",
+           "ep_dispatch_gather", "ep_swiglu")
 
 
 def load(build_if_missing: bool = True):
@@ -102,8 +113,12 @@ def load(build_if_missing: bool = True):
     L.grouped_gemm_combine_send_noalloc.argtypes = [ctypes.POINTER(ep_config),
                                                     ctypes.POINTER(ep_send_args), _vp]
     L.ep_scatter_send.argtypes = [ctypes.POINTER(ep_config), ctypes.POINTER(ep_scatter_args), _vp]
+    L.ep_dispatch_gather.argtypes = [ctypes.POINTER(ep_config), ctypes.POINTER(ep_dispatch_args),
+                                     _vp]
+    L.ep_swiglu.argtypes = [ctypes.POINTER(ep_config), ctypes.POINTER(ep_swiglu_args), _vp]
     for f in ("ep_plan_sizes", "ep_plan", "grouped_gemm_combine_send", "ep_combine_reduce",
-              "grouped_gemm_combine_send_noalloc", "ep_scatter_send"):
+              "grouped_gemm_combine_send_noalloc", "ep_scatter_send", "ep_dispatch_gather",
+              "ep_swiglu"):
         getattr(L, f).restype = ctypes.c_int
     L.ep_strerror.argtypes = [ctypes.c_int]
     L.ep_strerror.restype = ctypes.c_char_p
@@ -168,6 +183,18 @@ def ep_scatter_send(cfg: ep_config, args: ep_scatter_args, stream=None) -> int:
     buffers, then the count words and the rank flags."""
     return _check(load().ep_scatter_send(ctypes.byref(cfg), ctypes.byref(args),
                                          stream_handle(stream)), "ep_scatter_send")
+
+
+def ep_dispatch_gather(cfg: ep_config, args: ep_dispatch_args, stream=None) -> int:
+    """Dispatch: every routed token row to its expert's rank, in plan order."""
+    return _check(load().ep_dispatch_gather(ctypes.byref(cfg), ctypes.byref(args),
+                                            stream_handle(stream)), "ep_dispatch_gather")
+
+
+def ep_swiglu(cfg: ep_config, args: ep_swiglu_args, stream=None) -> int:
+    """A = bf16(SiLU(gate) * up) from the up/gate GEMM's rows."""
+    return _check(load().ep_swiglu(ctypes.byref(cfg), ctypes.byref(args),
+                                   stream_handle(stream)), "ep_swiglu")
 
 
 def ep_combine_reduce(cfg: ep_config, args: ep_combine_args, stream=None) -> int:

@@ -348,6 +348,64 @@ int ep_scatter_send(const ep_config *cfg, const ep_scatter_args *a, ep_stream_t 
     return cuda_status(ep::launch_scatter(p, num_sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int ep_dispatch_gather(const ep_config *cfg, const ep_dispatch_args *a, ep_stream_t stream)
+{
+    int rc = check_config(cfg);
+    if (rc != EP_OK)
+        return rc;
+    if (!a || !a->gather_idx || !a->expert_offsets || !a->A_in || !a->status)
+        return EP_ERR_INVALID_ARG;
+    if (a->hidden < 8 || a->hidden % 8 != 0 || !aligned16(a->A_in) || a->max_rows < 1 ||
+        a->max_rows > INT32_MAX)
+        return EP_ERR_INVALID_ARG;
+    ep::DispatchParams p;
+    std::memset(&p, 0, sizeof p);
+    for (int r = 0; r < cfg->n_ranks; ++r) {
+        if (!a->x_ptrs[r] || !aligned16(a->x_ptrs[r]))
+            return EP_ERR_INVALID_ARG;
+        p.x[r] = static_cast<const uint8_t *>(a->x_ptrs[r]);
+    }
+    const int num_sms = sm_count();
+    if (num_sms <= 0)
+        return EP_ERR_CUDA;
+    p.n_ranks = cfg->n_ranks;
+    p.El = cfg->n_local_experts;
+    p.top_k = cfg->top_k;
+    p.T = cfg->num_tokens;
+    p.max_tokens = cfg->max_tokens_per_rank;
+    p.hidden = a->hidden;
+    p.max_rows = a->max_rows;
+    p.gather_idx = a->gather_idx;
+    p.expert_offsets = a->expert_offsets;
+    p.A_in = static_cast<uint8_t *>(a->A_in);
+    p.status = a->status;
+    return cuda_status(
+        ep::launch_dispatch_gather(p, num_sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int ep_swiglu(const ep_config *cfg, const ep_swiglu_args *a, ep_stream_t stream)
+{
+    int rc = check_config(cfg);
+    if (rc != EP_OK)
+        return rc;
+    if (!a || !a->G || !a->A || !a->expert_offsets)
+        return EP_ERR_INVALID_ARG;
+    if (a->inter < 8 || a->inter % 8 != 0 || !aligned16(a->G) || !aligned16(a->A) ||
+        a->max_rows < 1 || a->max_rows > INT32_MAX)
+        return EP_ERR_INVALID_ARG;
+    const int num_sms = sm_count();
+    if (num_sms <= 0)
+        return EP_ERR_CUDA;
+    ep::SwigluParams p;
+    p.El = cfg->n_local_experts;
+    p.inter = a->inter;
+    p.max_rows = a->max_rows;
+    p.G = static_cast<const uint8_t *>(a->G);
+    p.A = static_cast<uint8_t *>(a->A);
+    p.expert_offsets = a->expert_offsets;
+    return cuda_status(ep::launch_swiglu(p, num_sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int ep_combine_reduce(const ep_config *cfg, const ep_combine_args *a, ep_stream_t stream)
 {
     int rc = check_config(cfg);

@@ -59,6 +59,25 @@ struct ScatterParams {
     int signal_mode;
 };
 
+// The layer steps around the fused down-projection (ep_layer.cu).
+struct DispatchParams {
+    int n_ranks, El, top_k, T, max_tokens, hidden;
+    int64_t max_rows;
+    const uint8_t *x[EP_MAX_RANKS];
+    const int32_t *gather_idx;
+    const int32_t *expert_offsets;
+    uint8_t *A_in;
+    uint32_t *status;
+};
+
+struct SwigluParams {
+    int El, inter;
+    int64_t max_rows;
+    const uint8_t *G;
+    uint8_t *A;
+    const int32_t *expert_offsets;
+};
+
 struct PlanParams {
     int n_ranks, my_rank, El, top_k, T;
     int64_t max_rows;
@@ -92,5 +111,7 @@ cudaError_t launch_gemm_send_bf16_pair(const CUtensorMap &ta, const CUtensorMap 
                                        const SendParams &p, int max_pairs, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_scatter(const ScatterParams &p, int num_sms, cudaStream_t s);
+cudaError_t launch_dispatch_gather(const DispatchParams &p, int num_sms, cudaStream_t s);
+cudaError_t launch_swiglu(const SwigluParams &p, int num_sms, cudaStream_t s);
 
 }  // namespace ep

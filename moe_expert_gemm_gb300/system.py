@@ -12,8 +12,9 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (EP_BF16, EP_FP8_1D2D, ep_combine_args, ep_combine_reduce, ep_config, ep_plan,
-               ep_plan_out, ep_plan_sizes, ep_scatter_args, ep_scatter_send, ep_send_args,
+from . import (EP_BF16, EP_FP8_1D2D, ep_combine_args, ep_combine_reduce, ep_config,
+               ep_dispatch_args, ep_dispatch_gather, ep_plan, ep_plan_out, ep_plan_sizes,
+               ep_scatter_args, ep_scatter_send, ep_send_args, ep_swiglu, ep_swiglu_args,
                grouped_gemm_combine_send, ptr)
 
 SENTINEL_BYTE = 0xFF  # received bf16 0xFFFF is a NaN: an unwritten slot cannot pass
@@ -168,6 +169,66 @@ class EpSystem:
         a.epoch = epoch
         a.status = self.status.data_ptr() + 4 * STATUS_SEND
         return a
+
+    # ------------------------------------------------------------ whole layer
+    def set_layer_operands(self, rank: int, X: np.ndarray, W1: np.ndarray, W2: np.ndarray):
+        """Operands of a whole MoE layer around the down-projection (bf16 bit
+        patterns): the rank's tokens X [T, H], its experts' up/gate weights W1
+        [E_l, 2I, H] (gate rows first) and down-projection weights W2 [E_l, H, I],
+        with H = N and I = K. The down-projection's A is produced on the device by
+        layer_forward (dispatch, up/gate GEMM, activation)."""
+        assert self.dtype == "bf16"
+        dev, H, I = self.device, self.N, self.K
+        x = torch.zeros((self.max_tokens, H), dtype=torch.int16)
+        x[:X.shape[0]] = torch.from_numpy(np.ascontiguousarray(X).view(np.int16))
+        rows = max(self.plans[rank]["capacity"], 1)
+        self.layer = getattr(self, "layer", [None] * self.R)
+        self.layer[rank] = dict(
+            X=x.view(torch.bfloat16).to(dev),
+            W1=torch.from_numpy(np.ascontiguousarray(W1).view(np.int16)).view(
+                torch.bfloat16).to(dev),
+            A_in=torch.zeros((rows, H), dtype=torch.bfloat16, device=dev),
+            G=torch.zeros((rows, 2 * I), dtype=torch.bfloat16, device=dev))
+        self.ops[rank] = dict(
+            A=torch.zeros((rows, I), dtype=torch.bfloat16, device=dev),
+            W=torch.from_numpy(np.ascontiguousarray(W2).view(np.int16)).view(
+                torch.bfloat16).to(dev))
+
+    def cfg_up(self, rank: int) -> ep_config:
+        """The up/gate projection's configuration: K = H, N = 2I."""
+        return ep_config(self.R, rank, self.El, self.k, self.T, self.max_tokens, self.N,
+                         2 * self.K, 4 * self.K, EP_BF16, self.send_warps, self.signal_mode)
+
+    def layer_forward(self, rank: int, epoch: int, stream=None, p3_control: int = 0,
+                      events=None):
+        """Dispatch, up/gate GEMM, activation, then the fused down-projection + send
+        of producer ``rank`` (every ``layer[r]["X"]`` must hold rank r's tokens).
+        ``events``: four CUDA events recorded after each of the first four steps."""
+        L, p = self.layer[rank], self.plans[rank]
+        mark = (lambda i: events[i].record(stream)) if events is not None else (lambda i: None)
+        d = ep_dispatch_args()
+        for r in range(self.R):
+            d.x_ptrs[r] = ptr(self.layer[r]["X"])
+        d.gather_idx = ptr(p["gather_idx"])
+        d.expert_offsets = ptr(p["expert_offsets"])
+        d.max_rows = int(L["A_in"].shape[0])
+        d.hidden = self.N
+        d.A_in = ptr(L["A_in"])
+        d.status = self.status.data_ptr() + 4 * STATUS_SEND
+        ep_dispatch_gather(self.cfg(rank), d, stream)
+        mark(0)
+        up = self.send_args(rank, epoch, -1, L["G"])
+        up.A = ptr(L["A_in"])
+        up.W = ptr(L["W1"])
+        up.max_rows = int(L["A_in"].shape[0])
+        grouped_gemm_combine_send(self.cfg_up(rank), up, stream)
+        mark(1)
+        a = ep_swiglu_args(ptr(L["G"]), ptr(self.ops[rank]["A"]), ptr(p["expert_offsets"]),
+                           int(L["G"].shape[0]), self.K)
+        ep_swiglu(self.cfg(rank), a, stream)
+        mark(2)
+        self.send(rank, epoch, stream, p3_control=p3_control)
+        mark(3)
 
     def send_traced(self, rank: int, epoch: int, records: int = 64, stream=None):
         """One send with per-tile timestamps; returns the decoded trace."""

@@ -253,6 +253,30 @@ def signal_per_expert(n_ranks: int, n_local_experts: int, rank: int, send_counts
     return np.array(log, np.int32).reshape(-1, 4)
 
 
+# ------------------------------------------------------------ layer steps
+
+def dispatch(pl: Plan, tokens: list, top_k: int) -> np.ndarray:
+    """The dispatch step before the down-projection's path: row m of the plan,
+    (source rank rk, token t, slot j) = gather_idx[m] = (rk*T + t)*top_k + j,
+    receives token row tokens[rk][t] unchanged (bf16 bit patterns)."""
+    T = tokens[0].shape[0]
+    out = np.zeros((pl.m_total, tokens[0].shape[1]), np.uint16)
+    for m in range(pl.m_total):
+        gi = int(pl.gather_idx[m])
+        rk, t = gi // (T * top_k), (gi % (T * top_k)) // top_k
+        out[m] = tokens[rk][t]
+    return out
+
+
+def swiglu(G_bits: np.ndarray, inter: int) -> np.ndarray:
+    """The gated activation: A[m][i] = bf16(SiLU(G[m][i]) * G[m][inter + i]) with
+    SiLU(x) = x / (1 + e^-x), evaluated in float64 on the bf16 values of G and
+    rounded to nearest even once."""
+    g = bf16_to_f64(np.ascontiguousarray(G_bits[:, :inter]))
+    u = bf16_to_f64(np.ascontiguousarray(G_bits[:, inter:2 * inter]))
+    return bf16_from_f64(g / (1.0 + np.exp(-g)) * u)
+
+
 # ------------------------------------------------------------------ combine
 
 def combine(recv_buf, gates, top_k: int, N: int, msg_bytes: int, tokens=None,

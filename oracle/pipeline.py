@@ -11,8 +11,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (BF16, FP8_1D2D, Plan, combine, combine_exact, default_threads, expert_rows, plan,
-               scatter, signal, signal_per_expert)
+from . import (BF16, FP8_1D2D, Plan, combine, combine_exact, default_threads, dispatch,
+               expert_rows, plan, scatter, signal, signal_per_expert, swiglu)
 
 SENTINEL_BYTE = 0xFF  # bf16 0xFFFF is a NaN: an unwritten slot cannot pass a value check
 SENTINEL_WORD = np.uint64(0xFFFFFFFFFFFFFFFF)
@@ -124,3 +124,30 @@ def sampled_pipeline(w, routing, values_of, dst: int, tokens, plans: dict | None
     out = combine(compact, g, k, N, 2 * N, threads=threads)
     return dict(tokens=tokens, rows=rows_out, where=where, out=out, plans=plans,
                 rows_exact=rows_exact, out_exact=combine_exact(rows_exact, g))
+
+
+def layer_pipeline(w, routing, layer_values: list, epoch: int = 1,
+                   threads: int | None = None) -> dict:
+    """A whole MoE layer around the down-projection (bf16): per producer rank, the
+    dispatch of its routed token rows, the up/gate projection (expert_rows with
+    K = H, N = 2I: rows rounded to bf16), the gated activation, then
+    ``full_pipeline`` on the resulting A and the down-projection weights.
+    ``layer_values[r]`` holds X, W1, W2 (``synth.make_layer_values``). Returns
+    ``full_pipeline``'s dict plus the intermediates A_in, G, A per rank."""
+    R, El, k = w.n_ranks, w.n_local_experts, w.top_k
+    H, I = w.N, w.K
+    tokens = [v["X"] for v in layer_values]
+    A_in, Gs, As, values = [], [], [], []
+    for r in range(R):
+        pl = plan(R, El, k, routing.topk_ids, r)
+        a_in = dispatch(pl, tokens, k)
+        G = expert_rows(BF16, a_in, layer_values[r]["W1"], pl.expert_offsets, H, 2 * I,
+                        threads=threads)
+        A = swiglu(G, I)
+        A_in.append(a_in)
+        Gs.append(G)
+        As.append(A)
+        values.append({"A": A, "W": layer_values[r]["W2"]})
+    res = full_pipeline(w, routing, values, epoch=epoch, threads=threads)
+    res.update(A_in=A_in, G=Gs, A=As)
+    return res

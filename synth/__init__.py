@@ -12,6 +12,7 @@ from .workloads import (  # noqa: F401
     Routing,
     make_routing,
     make_rank_values,
+    make_layer_values,
     rows_per_rank,
     bf16_bits_from_f32,
     e4m3_bits_from_f32,

@@ -49,6 +49,7 @@ import numpy as np
 _CHUNK = 1 << 22
 
 _TAG_A, _TAG_W, _TAG_SA, _TAG_SW = 1, 2, 3, 4
+_TAG_X, _TAG_W1 = 5, 6
 
 
 @dataclass(frozen=True)
@@ -246,4 +247,24 @@ def make_rank_values(w: Workload, rank: int, rows: int, seed: int | None = None)
                                               (base, _TAG_SW, rank)).reshape(El, N // 128, K // 128)
     else:
         raise ValueError(f"unknown dtype {w.dtype!r}")
+    return out
+
+
+def make_layer_values(w: Workload, rank: int, seed: int | None = None) -> dict:
+    """Operands of one rank for a whole MoE layer around the down-projection
+    (bf16 only): the rank's tokens ``X`` [T, H] (N(0, 1)), the up/gate weights of
+    its experts ``W1`` [E_l, 2I, H] (gate rows first, then up rows; N(0, 1)/sqrt(H))
+    and the down-projection weights ``W2`` [E_l, H, I] (as ``make_rank_values``'s
+    W). H = w.N (the hidden size the down-projection returns to), I = w.K (the
+    intermediate size it reads). uint16 bf16 bit patterns."""
+    if w.dtype != "bf16":
+        raise ValueError("the layer operands are bf16")
+    base = w.values_seed if seed is None else seed
+    H, I, El = w.N, w.K, w.n_local_experts
+    out = {"X": bf16_bits_from_f32(_normal(w.tokens * H, (base, _TAG_X, rank))).reshape(
+        w.tokens, H)}
+    out["W1"] = bf16_bits_from_f32(_normal(El * 2 * I * H, (base, _TAG_W1, rank))
+                                   * np.float32(1.0 / np.sqrt(H))).reshape(El, 2 * I, H)
+    out["W2"] = bf16_bits_from_f32(_normal(El * H * I, (base, _TAG_W, rank))
+                                   * np.float32(1.0 / np.sqrt(I))).reshape(El, H, I)
     return out

@@ -472,6 +472,42 @@ def test_fp8_identity_weights_move_data_exactly():
             np.testing.assert_array_equal(oracle.bf16_to_f64(res["out"][d][t]), want)
 
 
+def test_dispatch_places_every_token_row_by_the_brute_force_keys():
+    w = WORKLOADS["tiny"]
+    r = make_routing(w)
+    rng = np.random.default_rng(5)
+    tokens = [rng.integers(0, 2**16, (w.tokens, 24), dtype=np.uint16) for _ in range(w.n_ranks)]
+    for q in range(w.n_ranks):
+        pl = oracle.plan(w.n_ranks, w.n_local_experts, w.top_k, r.topk_ids, q)
+        A_in = oracle.dispatch(pl, tokens, w.top_k)
+        keys = _brute_plan(r.topk_ids, w.n_ranks, w.n_local_experts, q)
+        assert A_in.shape[0] == len(keys)
+        for m, (_, rk, t, _) in enumerate(keys):
+            np.testing.assert_array_equal(A_in[m], tokens[rk][t])
+
+
+def test_swiglu_matches_an_independent_form_and_special_values():
+    """SiLU(x) = x * sigmoid(x) = (x / 2) * (1 + tanh(x / 2)): a second form of the
+    same function, evaluated independently; plus values fixed by the definition."""
+    rng = np.random.default_rng(8)
+    inter = 64
+    g32 = (rng.standard_normal((50, inter)) * 4).astype(np.float32)
+    u32 = rng.standard_normal((50, inter)).astype(np.float32)
+    G = _torch_bf16_bits(np.concatenate([g32, u32], axis=1))
+    A = oracle.swiglu(G, inter)
+    g = oracle.bf16_to_f64(G[:, :inter])
+    u = oracle.bf16_to_f64(G[:, inter:])
+    want = oracle.bf16_from_f64(0.5 * g * (1.0 + np.tanh(0.5 * g)) * u)
+    diff = np.abs(oracle.bf16_to_f64(A) - oracle.bf16_to_f64(want))
+    assert (diff <= 2.0**-8 * np.abs(oracle.bf16_to_f64(want)) + 1e-30).all()
+    assert (A == want).mean() > 0.999  # the two forms round alike except at rare ties
+    # the gate selects: SiLU(0) = 0; SiLU(large) ~ large; SiLU(-large) ~ 0; the up half scales
+    G2 = _torch_bf16_bits(np.array([[0.0, 30.0, -30.0, 1.0, 3.0, 3.0, 3.0, 0.0]], np.float32))
+    A2 = oracle.bf16_to_f64(oracle.swiglu(G2, 4))[0]
+    assert A2[0] == 0.0 and A2[3] == 0.0
+    assert abs(A2[1] - 90.0) <= 0.5 and abs(A2[2]) < 1e-9
+
+
 def test_sampled_pipeline_agrees_with_full():
     w, r, vals, res = _tiny_full()
     toks = np.array([0, 5, 63, 17])
