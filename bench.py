@@ -69,6 +69,9 @@ def parse_args():
                     help="unfused: the comparator without the sink (GEMM rows to a local C, "
                          "then ep_scatter_send); layer: a whole MoE layer (dispatch, up/gate "
                          "GEMM, activation, the fused down-projection + send, combine; bf16)")
+    ap.add_argument("--layer-act", choices=["fused", "separate"], default="fused",
+                    help="--path layer: the activation in the up/gate GEMM's epilogue (fused) "
+                         "or as its own pass over the GEMM's rows (separate)")
     ap.add_argument("--signal-mode", choices=["rank_flag", "per_expert"], default="rank_flag",
                     help="completion signalling: ep_ord_r rank flags (default) or per-expert "
                          "count words with a per-token wait in the combine")
@@ -345,7 +348,7 @@ def main():
     # peers' rows land in every receive buffer once (their producers are not timed)
     for r in ranks:
         if layer:
-            s.layer_forward(r, epoch=1)
+            s.layer_forward(r, epoch=1, fused_act=args.layer_act == "fused")
         else:
             s.send(r, epoch=1)
     torch.cuda.synchronize()
@@ -393,7 +396,8 @@ def main():
             evs[0].record(stream)
         if layer:
             s.layer_forward(q, e, stream, events=None if evs is None
-                            else [evs[4], evs[5], evs[6], evs[7]])
+                            else [evs[4], evs[5], evs[6], evs[7]],
+                            fused_act=args.layer_act == "fused")
         elif unfused:
             s.send(q, e, stream, p3_control=-1, C=C_local)
             if evs is not None:
@@ -540,7 +544,7 @@ def main():
     if layer:
         flops = 2.0 * m_rows * w.N * 2 * w.K
         send_bytes = m_rows * w.N * 2 + plan_q["send_counts"].shape[0] * 2 * w.K * w.N * 2 \
-            + m_rows * 2 * w.K * 2
+            + m_rows * (1 if args.layer_act == "fused" else 2) * w.K * 2
         dom_s = stage_ms[1] / 1e3
     else:
         dom_s = statistics.mean(gemm_ms) / 1e3 if unfused else send_s
@@ -602,6 +606,7 @@ def main():
         line["config"]["solo"] = "profiling aid: fused send only, peers not staged"
     if layer:
         line["config"]["layer"] = {"hidden": w.N, "intermediate": w.K,
+                                   "activation": args.layer_act,
                                    "metric": "tokens/s of the whole layer for one rank"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.solo and not layer:
         import oracle

@@ -202,7 +202,19 @@ int ep_plan(const ep_config *cfg, const int32_t *topk_ids, const ep_plan_out *ou
  *                    each records it.
  *   timeout_ns       limit of each bounded wait inside the kernel (0: 2 s).
  *   trace_records    records per thread block in `trace` (>= 1 when trace is set).
+ *   local_activation with p3_control < 0 only (else ignored): EP_ACT_NONE stores the
+ *                    rows as they are; EP_ACT_SWIGLU makes the call the up/gate
+ *                    projection of a gated MLP with the activation in its epilogue:
+ *                    W's rows come in interleaved 128-row blocks (rows 256b..256b+127
+ *                    are the gate rows of intermediate indices 128b..128b+127, the next
+ *                    128 rows the up rows of the same indices), and C receives
+ *                    [max_rows][N/2] bf16 rows bf16(SiLU(gate) * up) computed from the
+ *                    fp32 accumulators (SiLU(x) = x / (1 + e^-x), fp32). Needs bf16,
+ *                    N % 256 == 0 and send_warps != 4, else EP_ERR_UNSUPPORTED.
  */
+#define EP_ACT_NONE 0
+#define EP_ACT_SWIGLU 1
+
 typedef struct {
     const void *A;
     const float *a_scales;
@@ -224,6 +236,7 @@ typedef struct {
     uint64_t *trace;
     int64_t timeout_ns;
     int64_t trace_records;
+    int32_t local_activation;
 } ep_send_args;
 
 /*

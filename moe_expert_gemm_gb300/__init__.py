@@ -25,6 +25,8 @@ EP_ERR_CUDA = -3
 EP_STATUS_BOUNDS = 0x1
 EP_STATUS_TIMEOUT = 0x2
 EP_STATUS_CAPACITY = 0x4
+EP_ACT_NONE = 0
+EP_ACT_SWIGLU = 1
 EP_SIGNAL_RANK_FLAG = 0
 EP_SIGNAL_PER_EXPERT = 1
 EP_STATUS_ROUTING = 0x8
@@ -55,7 +57,8 @@ class ep_send_args(ctypes.Structure):
                 ("recv_buf_ptrs", _vp * EP_MAX_RANKS), ("recv_count_ptrs", _vp * EP_MAX_RANKS),
                 ("atomic_counter", _vp), ("rank_completion_counter", _vp), ("epoch", _c_u64),
                 ("p3_control", _c_i32), ("C", _vp), ("status", _vp), ("trace", _vp),
-                ("timeout_ns", _c_i64), ("trace_records", _c_i64)]
+                ("timeout_ns", _c_i64), ("trace_records", _c_i64),
+                ("local_activation", _c_i32)]
 
 
 class ep_combine_args(ctypes.Structure):

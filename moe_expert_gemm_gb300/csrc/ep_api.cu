@@ -187,6 +187,13 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     // dedicated send warps exist in the single-CTA bf16 kernel
     if (fp8 && cfg->send_warps == 4)
         return EP_ERR_UNSUPPORTED;
+    if (a->p3_control < 0 && a->local_activation != EP_ACT_NONE) {
+        if (a->local_activation != EP_ACT_SWIGLU)
+            return EP_ERR_INVALID_ARG;
+        // the activation pairs the two 128-column halves of a 256-column tile
+        if (fp8 || cfg->N % 256 != 0 || cfg->send_warps == 4)
+            return EP_ERR_UNSUPPORTED;
+    }
     if (!fp8 && (cfg->K % 64 != 0 || cfg->N % 64 != 0))
         return EP_ERR_UNSUPPORTED;  // whole 128-byte K atoms and 64-column output chunks
     // fp8: one 128-wide scale block per K step, whole 128-column weight-scale blocks
@@ -276,6 +283,8 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     p.epoch = a->epoch;
     p.sink_enabled = sink ? 1 : 0;
     p.signal_mode = cfg->signal_mode;
+    p.act_swiglu = !sink && a->local_activation == EP_ACT_SWIGLU ? 1 : 0;
+    p.c_row_bytes = static_cast<int64_t>(cfg->N) * (p.act_swiglu ? 1 : 2);
     p.C = static_cast<uint8_t *>(a->C);
     p.status = a->status;
     p.timeout_ns = a->timeout_ns > 0 ? static_cast<uint64_t>(a->timeout_ns) : kDefaultTimeoutNs;

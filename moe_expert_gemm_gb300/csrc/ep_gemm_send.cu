@@ -232,6 +232,7 @@ __global__ void __launch_bounds__(224 + 32 * SEND, 1)
         bool push_ok = true;  // epi_tid 0: the last hand-off to the completion warp succeeded
                               // (SEND: every wait of this warp for a free slot succeeded)
         int k_sub = 0;        // SEND: sub-tiles this warp has handed to its send warp
+        const bool act = SEND == 0 && p.act_swiglu;  // gated-MLP epilogue (local C only)
         int i = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++i) {
             const TileCoord c = decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks, BM, p.m_fastest);
@@ -256,14 +257,32 @@ __global__ void __launch_bounds__(224 + 32 * SEND, 1)
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(as * BN);
 #pragma unroll 1
-            for (int sub = 0; sub < BN / 64; ++sub) {
+            for (int sub = 0; sub < (act ? BN / 128 : BN / 64); ++sub) {
                 uint32_t v0[32], v1[32];
                 tmem_ld_32x32b_x32(t_row + sub * 64, v0);
                 tmem_ld_32x32b_x32(t_row + sub * 64 + 32, v1);
-                tmem_ld_wait();
-                tmem_regs_ready(v0);
-                tmem_regs_ready(v1);
-                const int col_byte = (c.nb * BN + sub * 64) * 2;
+                if (act) {
+                    // gated MLP: this sub-tile's gate columns and, BN/2 further on, the
+                    // up columns of the same intermediate indices
+                    uint32_t u0[32], u1[32];
+                    tmem_ld_32x32b_x32(t_row + BN / 2 + sub * 64, u0);
+                    tmem_ld_32x32b_x32(t_row + BN / 2 + sub * 64 + 32, u1);
+                    tmem_ld_wait();
+                    tmem_regs_ready(v0);
+                    tmem_regs_ready(v1);
+                    tmem_regs_ready(u0);
+                    tmem_regs_ready(u1);
+#pragma unroll
+                    for (int c2 = 0; c2 < 32; ++c2) {
+                        swiglu_inplace(v0[c2], u0[c2]);
+                        swiglu_inplace(v1[c2], u1[c2]);
+                    }
+                } else {
+                    tmem_ld_wait();
+                    tmem_regs_ready(v0);
+                    tmem_regs_ready(v1);
+                }
+                const int col_byte = (c.nb * (act ? BN / 2 : BN) + sub * 64) * 2;
                 uint32_t buf = stg;
                 int slot = 0;
                 if constexpr (SEND != 0) {

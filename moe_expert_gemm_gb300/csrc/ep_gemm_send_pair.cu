@@ -223,6 +223,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
 
         bool ok = true;
         bool push_ok = true;
+        const bool act = p.act_swiglu != 0;  // gated-MLP epilogue (local C only)
         int i = 0;
         for (int t = pair; t < total_tiles; t += n_pairs, ++i) {
             const TileCoord c =
@@ -246,13 +247,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(as * BN);
 #pragma unroll 1
-            for (int sub = 0; sub < BN / 64; ++sub) {
+            for (int sub = 0; sub < (act ? BN / 128 : BN / 64); ++sub) {
                 uint32_t v0[32], v1[32];
                 tmem_ld_32x32b_x32(t_row + sub * 64, v0);
                 tmem_ld_32x32b_x32(t_row + sub * 64 + 32, v1);
-                tmem_ld_wait();
-                tmem_regs_ready(v0);
-                tmem_regs_ready(v1);
+                if (act) {
+                    // gated MLP: this sub-tile's gate columns and, BN/2 further on, the
+                    // up columns of the same intermediate indices
+                    uint32_t u0[32], u1[32];
+                    tmem_ld_32x32b_x32(t_row + BN / 2 + sub * 64, u0);
+                    tmem_ld_32x32b_x32(t_row + BN / 2 + sub * 64 + 32, u1);
+                    tmem_ld_wait();
+                    tmem_regs_ready(v0);
+                    tmem_regs_ready(v1);
+                    tmem_regs_ready(u0);
+                    tmem_regs_ready(u1);
+#pragma unroll
+                    for (int c2 = 0; c2 < 32; ++c2) {
+                        swiglu_inplace(v0[c2], u0[c2]);
+                        swiglu_inplace(v1[c2], u1[c2]);
+                    }
+                } else {
+                    tmem_ld_wait();
+                    tmem_regs_ready(v0);
+                    tmem_regs_ready(v1);
+                }
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     const uint32_t *v = ch < 4 ? v0 + ch * 8 : v1 + (ch - 4) * 8;
@@ -267,7 +286,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
                                  make_uint4(w[0], w[1], w[2], w[3]));
                 }
                 __syncwarp();
-                const int col_byte = (c.nb * BN + sub * 64) * 2;
+                const int col_byte = (c.nb * (act ? BN / 2 : BN) + sub * 64) * 2;
 #pragma unroll
                 for (int it = 0; it < 8; ++it) {
                     const int row = it * 4 + (lane >> 3);

@@ -32,6 +32,8 @@ struct SendParams {
     uint64_t epoch;
     int sink_enabled;  // p3_control >= 0
     int signal_mode;   // EP_SIGNAL_RANK_FLAG or EP_SIGNAL_PER_EXPERT
+    int act_swiglu;    // sink disabled: gate/up column halves -> SiLU(gate) * up
+    int64_t c_row_bytes;  // local C row pitch (N*2, or N with the activation)
     uint8_t *C;        // local output when the sink is disabled
     uint32_t *status;
     uint64_t timeout_ns;

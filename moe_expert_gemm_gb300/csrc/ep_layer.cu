@@ -43,12 +43,6 @@ __global__ void __launch_bounds__(kLayerThreads) dispatch_gather_kernel(const Di
         atomicOr(p.status, EP_STATUS_BOUNDS);
 }
 
-// SiLU(x) = x / (1 + e^-x), in fp32 (expf of the CUDA math library).
-__device__ __forceinline__ float silu(float x)
-{
-    return x / (1.f + expf(-x));
-}
-
 // A[m][i] = bf16( SiLU(G[m][i]) * G[m][I + i] ) for i < I, m < m_total: the gate
 // half first, the up half second.
 __global__ void __launch_bounds__(kLayerThreads) swiglu_kernel(const SwigluParams p)
@@ -72,7 +66,7 @@ __global__ void __launch_bounds__(kLayerThreads) swiglu_kernel(const SwigluParam
             for (int h = 0; h < 4; ++h) {
                 const float g0 = __uint_as_float(gw[h] << 16), g1 = __uint_as_float(gw[h] & 0xFFFF0000u);
                 const float u0 = __uint_as_float(uw[h] << 16), u1 = __uint_as_float(uw[h] & 0xFFFF0000u);
-                __nv_bfloat162 b = __float22bfloat162_rn(make_float2(silu(g0) * u0, silu(g1) * u1));
+                __nv_bfloat162 b = __float22bfloat162_rn(make_float2(silu_f32(g0) * u0, silu_f32(g1) * u1));
                 o[h] = *reinterpret_cast<uint32_t *>(&b);
             }
             out[c] = make_uint4(o[0], o[1], o[2], o[3]);

@@ -432,6 +432,19 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t *bar, uint16_t mask)
         : "memory");
 }
 
+// SiLU(x) = x / (1 + e^-x) in fp32 (expf of the CUDA math library).
+__device__ __forceinline__ float silu_f32(float x)
+{
+    return x / (1.f + expf(-x));
+}
+
+// Gated activation of one accumulator column pair, in place on the gate word:
+// gate <- SiLU(gate) * up (fp32 bit patterns).
+__device__ __forceinline__ void swiglu_inplace(uint32_t &gate, uint32_t up)
+{
+    gate = __float_as_uint(silu_f32(__uint_as_float(gate)) * __uint_as_float(up));
+}
+
 // ------------------------------------------------------------ scoped memory ops
 
 __device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v)

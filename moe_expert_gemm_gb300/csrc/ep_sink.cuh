@@ -206,7 +206,7 @@ __device__ __forceinline__ uint8_t *resolve_row(const SendParams &p, const SinkS
     if (m >= c.m_end)
         return nullptr;
     if (!p.sink_enabled)
-        return p.C + static_cast<int64_t>(m) * p.N * 2;
+        return p.C + static_cast<int64_t>(m) * p.c_row_bytes;
     const int R = p.n_ranks;
     const int *seg = p.seg_offsets + c.e * (R + 1);
     int dst = -1;

@@ -12,7 +12,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (EP_BF16, EP_FP8_1D2D, ep_combine_args, ep_combine_reduce, ep_config,
+from . import (EP_ACT_SWIGLU, EP_BF16, EP_FP8_1D2D, ep_combine_args, ep_combine_reduce, ep_config,
                ep_dispatch_args, ep_dispatch_gather, ep_plan, ep_plan_out, ep_plan_sizes,
                ep_scatter_args, ep_scatter_send, ep_send_args, ep_swiglu, ep_swiglu_args,
                grouped_gemm_combine_send, ptr)
@@ -183,9 +183,15 @@ class EpSystem:
         x[:X.shape[0]] = torch.from_numpy(np.ascontiguousarray(X).view(np.int16))
         rows = max(self.plans[rank]["capacity"], 1)
         self.layer = getattr(self, "layer", [None] * self.R)
+        w1 = np.ascontiguousarray(W1).view(np.int16)
+        # the same rows in 128-row gate/up blocks, for the activation in the epilogue
+        El = w1.shape[0]
+        w1i = w1.reshape(El, 2, I // 128, 128, H).transpose(0, 2, 1, 3, 4).reshape(El, 2 * I, H) \
+            if I % 128 == 0 else None
         self.layer[rank] = dict(
             X=x.view(torch.bfloat16).to(dev),
-            W1=torch.from_numpy(np.ascontiguousarray(W1).view(np.int16)).view(
+            W1=torch.from_numpy(w1).view(torch.bfloat16).to(dev),
+            W1i=None if w1i is None else torch.from_numpy(np.ascontiguousarray(w1i)).view(
                 torch.bfloat16).to(dev),
             A_in=torch.zeros((rows, H), dtype=torch.bfloat16, device=dev),
             G=torch.zeros((rows, 2 * I), dtype=torch.bfloat16, device=dev))
@@ -200,10 +206,12 @@ class EpSystem:
                          2 * self.K, 4 * self.K, EP_BF16, self.send_warps, self.signal_mode)
 
     def layer_forward(self, rank: int, epoch: int, stream=None, p3_control: int = 0,
-                      events=None):
+                      events=None, fused_act: bool = False):
         """Dispatch, up/gate GEMM, activation, then the fused down-projection + send
         of producer ``rank`` (every ``layer[r]["X"]`` must hold rank r's tokens).
-        ``events``: four CUDA events recorded after each of the first four steps."""
+        ``fused_act``: the activation runs in the up/gate GEMM's epilogue (interleaved
+        W1, no G) instead of as its own pass. ``events``: four CUDA events recorded
+        after each of the first four steps."""
         L, p = self.layer[rank], self.plans[rank]
         mark = (lambda i: events[i].record(stream)) if events is not None else (lambda i: None)
         d = ep_dispatch_args()
@@ -217,15 +225,18 @@ class EpSystem:
         d.status = self.status.data_ptr() + 4 * STATUS_SEND
         ep_dispatch_gather(self.cfg(rank), d, stream)
         mark(0)
-        up = self.send_args(rank, epoch, -1, L["G"])
+        up = self.send_args(rank, epoch, -1, self.ops[rank]["A"] if fused_act else L["G"])
         up.A = ptr(L["A_in"])
-        up.W = ptr(L["W1"])
+        up.W = ptr(L["W1i"] if fused_act else L["W1"])
         up.max_rows = int(L["A_in"].shape[0])
+        if fused_act:
+            up.local_activation = EP_ACT_SWIGLU
         grouped_gemm_combine_send(self.cfg_up(rank), up, stream)
         mark(1)
-        a = ep_swiglu_args(ptr(L["G"]), ptr(self.ops[rank]["A"]), ptr(p["expert_offsets"]),
-                           int(L["G"].shape[0]), self.K)
-        ep_swiglu(self.cfg(rank), a, stream)
+        if not fused_act:
+            a = ep_swiglu_args(ptr(L["G"]), ptr(self.ops[rank]["A"]),
+                               ptr(p["expert_offsets"]), int(L["G"].shape[0]), self.K)
+            ep_swiglu(self.cfg(rank), a, stream)
         mark(2)
         self.send(rank, epoch, stream, p3_control=p3_control)
         mark(3)

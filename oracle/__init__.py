@@ -277,6 +277,14 @@ def swiglu(G_bits: np.ndarray, inter: int) -> np.ndarray:
     return bf16_from_f64(g / (1.0 + np.exp(-g)) * u)
 
 
+def swiglu_exact(G: np.ndarray, inter: int) -> np.ndarray:
+    """The same activation applied to the unrounded (float64) products, as the
+    up/gate projection with the activation in its epilogue computes it: the gate
+    and up values are never rounded to bf16, only the result is."""
+    g, u = G[:, :inter], G[:, inter:2 * inter]
+    return bf16_from_f64(g / (1.0 + np.exp(-g)) * u)
+
+
 # ------------------------------------------------------------------ combine
 
 def combine(recv_buf, gates, top_k: int, N: int, msg_bytes: int, tokens=None,
