@@ -24,15 +24,26 @@ MEDIUM = {
 }
 
 
-@pytest.mark.parametrize("name", ["mixtral_prefill", "dsv3_decode", "qwen3_skew",
-                                  "dsv3_prefill_fp8", "fp8_rows_fastest"])
-def test_full_size_sampled_parity(name):
+CASES = [(n, "fused", 0) for n in ("mixtral_prefill", "dsv3_decode", "qwen3_skew",
+                                   "dsv3_prefill_fp8", "fp8_rows_fastest")] + [
+    # the other producer and signalling forms at full size
+    ("qwen3_skew", "unfused", 0), ("dsv3_decode", "fused", 1), ("mixtral_prefill", "unfused", 1),
+    ("dsv3_prefill_fp8", "fused", 1)]
+
+
+@pytest.mark.parametrize("name,path,signal_mode", CASES,
+                         ids=[f"{n}-{p}-{'per_expert' if m else 'rank_flag'}"
+                              for n, p, m in CASES])
+def test_full_size_sampled_parity(name, path, signal_mode):
     w = WORKLOADS[name] if name in WORKLOADS else MEDIUM[name]
     R, El, k, T, N = w.n_ranks, w.n_local_experts, w.top_k, w.tokens, w.N
     routing, values = make_inputs(w)
-    s = build_system(w, routing, values)
+    s = build_system(w, routing, values, signal_mode=signal_mode)
     for r in range(R):
-        s.send(r, epoch=1)
+        if path == "unfused":
+            s.send_unfused(r, 1, s.local_C(r))
+        else:
+            s.send(r, epoch=1)
     s.combine(0, epoch=1)
     torch.cuda.synchronize()
     st = s.status_words()
@@ -43,7 +54,10 @@ def test_full_size_sampled_parity(name):
         assert_plan_equal(s.plan_host(r), plans[r])
     counts = [np.full(El * R + R, SENTINEL_WORD, np.uint64) for _ in range(R)]
     for r in range(R):
-        oracle.signal(R, El, r, plans[r].send_counts, 1, counts, np.zeros(R, np.int32))
+        if signal_mode:
+            oracle.signal_per_expert(R, El, r, plans[r].send_counts, 1, counts)
+        else:
+            oracle.signal(R, El, r, plans[r].send_counts, 1, counts, np.zeros(R, np.int32))
     for d in range(R):
         np.testing.assert_array_equal(s.counts[d].cpu().numpy().view(np.uint64), counts[d])
 
