@@ -155,14 +155,23 @@ FUSED_KERNEL_SOURCES = ("ep_api.cu", "ep_gemm_send.cu", "ep_gemm_send_fp8.cu",
                         "ep_gemm_send_pair.cu", "ep_internal.h", "ep_ptx.cuh", "ep_sink.cuh")
 
 
+def _code_only(text: str) -> str:
+    """C++ source without its comments and blank lines (a comment edit does not
+    change what a measurement describes)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_sha() -> str:
-    """Digest of the fused kernels' sources (a measurement taken on other sources
-    does not describe the current kernels)."""
+    """Digest of the fused kernels' code (a measurement taken on other code does not
+    describe the current kernels)."""
     csrc = os.path.join(ROOT, "moe_expert_gemm_gb300", "csrc")
     h = hashlib.sha256()
     for name in FUSED_KERNEL_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -241,15 +241,18 @@ typedef struct {
 
 /*
  * One persistent kernel: for every local expert e and every 128-row tile of its
- * rows and every column block, Y_e = A_e * W_e^T on the tensor cores (fp32
- * accumulation), rounded to bf16 and written row by row to the receive buffer of
- * the rank that owns each row's token. No local C tensor exists ("EpiloguePeerSink"
- * Enabled: the local store and its TMA descriptor are dead).
- * When the last tile of expert e is done, for every destination rank dst: a plain
- * store of the count word, then an acquire-release increment of
+ * rows (256-row tiles on CTA pairs, bf16) and every column block, Y_e = A_e * W_e^T
+ * on the tensor cores (fp32 accumulation), rounded to bf16 and written row by row to
+ * the receive buffer of the rank that owns each row's token. No local C tensor
+ * exists ("EpiloguePeerSink" Enabled: the local store and its TMA descriptor are
+ * dead).
+ * EP_SIGNAL_RANK_FLAG: when the last tile of expert e is done, for every destination
+ * rank dst: a plain store of the count word, then an acquire-release increment of
  * rank_completion_counter[dst]; the call that sees E_l-1 release-stores (system
  * scope) `epoch` into dst's flag word for my_rank ("ep_signal_completion",
- * ep_ord_r with has_rank_flag). Experts with no rows signal count 0.
+ * ep_ord_r with has_rank_flag). EP_SIGNAL_PER_EXPERT: the count words, tagged with
+ * the epoch, are released for each expert; no election, no flag. Experts with no
+ * rows signal count 0.
  */
 int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *args,
                               ep_stream_t stream);

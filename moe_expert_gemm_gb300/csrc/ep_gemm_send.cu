@@ -22,6 +22,11 @@
 // epilogue warps, the finished tile goes to warp 6, which counts tiles per expert
 // and runs the completion signalling, off the output path.
 //
+// Variants: SEND = 4 adds four send warps (7-10) that store the rows the epilogue
+// warps stage in two slots each ("EpiloguePeerSink" SendWarps). With the sink
+// disabled the rows go to the local C, optionally through the gated activation
+// (act_swiglu: each sub-tile pairs gate columns with the up columns BN/2 further on).
+//
 // Every wait is bounded (timeout_ns of %globaltimer): on expiry the kernel sets
 // EP_STATUS_TIMEOUT, the other roles stop at their next wait, outstanding TMA
 // loads and MMAs are waited for (again bounded), TMEM is freed and the CTA exits.
