@@ -72,6 +72,9 @@ def parse_args():
     ap.add_argument("--layer-act", choices=["fused", "separate"], default="fused",
                     help="--path layer: the activation in the up/gate GEMM's epilogue (fused) "
                          "or as its own pass over the GEMM's rows (separate)")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="launch the combine after the fused send has ended instead of as a "
+                         "programmatic dependent that starts while the send finishes")
     ap.add_argument("--signal-mode", choices=["rank_flag", "per_expert"], default="rank_flag",
                     help="completion signalling: ep_ord_r rank flags (default) or per-expert "
                          "count words with a per-token wait in the combine")
@@ -395,7 +398,12 @@ def main():
     unfused = args.path == "unfused"
     C_local = s.local_C(q) if unfused else None
 
-    def one_step(evs=None):
+    # the combine may start while the fused send finishes (its rows are ordered by the
+    # flags it acquires, not by the kernel boundary); the per-kernel breakdown is taken
+    # from separately timed steps with the two kernels serialised
+    overlap = not args.no_overlap and not unfused and not layer
+
+    def one_step(evs=None, serial=False):
         e = epoch[0]
         epoch[0] += 1
         if flush is not None:
@@ -414,10 +422,10 @@ def main():
             ep.ep_scatter_send(s.cfg(q), s.scatter_args(q, e, C_local), stream)
         else:
             s.send(q, e, stream)
-        if evs is not None:
+        if evs is not None and (serial or not overlap):
             evs[1].record(stream)
         if not args.solo:
-            s.combine(q, e, stream)
+            s.combine(q, e, stream, overlap=overlap and not serial)
         if evs is not None:
             evs[2].record(stream)
 
@@ -436,6 +444,14 @@ def main():
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
+    step_overlapped = (statistics.mean(e[0].elapsed_time(e[2]) for e in events)
+                       if overlap else None)
+    if overlap:  # per-kernel times: the same steps with the kernels serialised
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(8)]
+                  for _ in range(args.steps)]
+        for i in range(args.steps):
+            one_step(events[i], serial=True)
+        torch.cuda.synchronize()
     clk = clocks.stop()
     send_ms = [e[0].elapsed_time(e[1]) for e in events]
     comb_ms = [e[1].elapsed_time(e[2]) for e in events]
@@ -443,7 +459,7 @@ def main():
     if layer:  # dispatch, up/gate GEMM, activation, fused down-projection + send
         stage_ms = [statistics.mean(e[a].elapsed_time(e[b]) for e in events)
                     for a, b in ((0, 4), (4, 5), (5, 6), (6, 7))]
-    step_ms = sum(a + b for a, b in zip(send_ms, comb_ms)) / args.steps
+    step_ms = step_overlapped if overlap else sum(a + b for a, b in zip(send_ms, comb_ms)) / args.steps
     st = s.status_words()
     if st.any():
         raise SystemExit(f"device status after timing: {st}")
@@ -504,7 +520,8 @@ def main():
             if fp8:
                 a.a_scales = ep.ptr(sa_bufs[b])
             ep.grouped_gemm_combine_send(cfg_q, a, stream)
-            ep.ep_combine_reduce(cfg_q, s.combine_args(q, e, gates=g_bufs[b], out=o_bufs[b]),
+            ep.ep_combine_reduce(cfg_q, s.combine_args(q, e, gates=g_bufs[b], out=o_bufs[b],
+                                                       overlap=overlap),
                                  stream)
             inputs_free[b] = stream.record_event()
             d2h_stream.wait_event(inputs_free[b])
@@ -589,6 +606,7 @@ def main():
                    "top_k": w.top_k, "tokens_per_rank": w.tokens, "K": w.K, "N": w.N,
                    "operands": w.dtype, "my_rank": q, "rows": m_rows,
                    "send_warps": args.send_warps, "path": args.path,
+                   "combine_overlaps_send": overlap,
                    "signal_mode": args.signal_mode,
                    "l2": ("flushed with a 512 MB write before every step" if flush is not None
                           else f"per-step inputs {step_bytes / 1e6:.0f} MB > L2"),

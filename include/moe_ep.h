@@ -397,6 +397,12 @@ int ep_swiglu(const ep_config *cfg, const ep_swiglu_args *args, ep_stream_t stre
  *               and the affected outputs are left unwritten
  *   topk_ids    EP_SIGNAL_PER_EXPERT only: this rank's routing, [num_tokens][top_k]
  *               global expert ids (the table ep_plan reads, rank my_rank's part)
+ *   overlap_previous  nonzero: launch as a programmatic dependent of the previous
+ *               kernel on `stream`, so that when that kernel is this library's fused
+ *               send (which signals its dependents as its thread blocks finish) the
+ *               combine starts before the send has fully ended. Safe because the
+ *               combine reads no row before acquiring the signal that releases it;
+ *               after any other kernel it simply waits for its completion.
  * EP_SIGNAL_RANK_FLAG: each thread block acquires every source rank's flag once
  * (system scope) before reading the rows, as the fused consumer of
  * "ep_signal_completion" does. EP_SIGNAL_PER_EXPERT: before reducing a token, the
@@ -412,6 +418,7 @@ typedef struct {
     int64_t timeout_ns;
     uint32_t *status;
     const int32_t *topk_ids;
+    int32_t overlap_previous;
 } ep_combine_args;
 
 int ep_combine_reduce(const ep_config *cfg, const ep_combine_args *args, ep_stream_t stream);

@@ -64,7 +64,7 @@ class ep_send_args(ctypes.Structure):
 class ep_combine_args(ctypes.Structure):
     _fields_ = [("recv_buf", _vp), ("recv_count", _vp), ("gates", _vp), ("out", _vp),
                 ("epoch", _c_u64), ("timeout_ns", _c_i64), ("status", _vp),
-                ("topk_ids", _vp)]
+                ("topk_ids", _vp), ("overlap_previous", _c_i32)]
 
 
 class ep_scatter_args(ctypes.Structure):

@@ -448,6 +448,7 @@ int ep_combine_reduce(const ep_config *cfg, const ep_combine_args *a, ep_stream_
     p.status = a->status;
     p.topk_ids = a->topk_ids;
     p.signal_mode = cfg->signal_mode;
+    p.overlap_previous = a->overlap_previous != 0 ? 1 : 0;
     return cuda_status(ep::launch_combine(p, num_sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -298,6 +298,24 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel_any(const Comb
     }
 }
 
+// Launch; with overlap_previous as a programmatic dependent of the previous kernel
+// on the stream (it may start once that kernel's thread blocks have signalled).
+static cudaError_t launch_with(void (*kern)(CombineParams), int blocks, const CombineParams &p,
+                               cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks, 1, 1);
+    cfg.blockDim = dim3(kCombineThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.overlap_previous ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 template <typename Kern>
 static int blocks_for(Kern kern, int num_sms, int64_t work_blocks)
 {
@@ -319,8 +337,7 @@ static cudaError_t launch_k(const CombineParams &p, int num_sms, cudaStream_t s)
     constexpr int U = K >= kLoads ? 1 : kLoads / K;
     const int64_t units = static_cast<int64_t>(p.T) * ((p.N / 8 + 31) / 32);
     const int b = blocks_for(combine_kernel<K>, num_sms, (units + 8 * U - 1) / (8 * U));
-    combine_kernel<K><<<b, kCombineThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_with(combine_kernel<K>, b, p, s);
 }
 
 template <int K>
@@ -329,8 +346,7 @@ static cudaError_t launch_per_expert(const CombineParams &p, int num_sms, cudaSt
     constexpr int U = K == 0 ? 1 : (K >= kLoads ? 1 : kLoads / K);
     const int64_t units = static_cast<int64_t>(p.T) * ((p.N / 8 + 31) / 32);
     const int b = blocks_for(combine_kernel_per_expert<K>, num_sms, (units + 8 * U - 1) / (8 * U));
-    combine_kernel_per_expert<K><<<b, kCombineThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_with(combine_kernel_per_expert<K>, b, p, s);
 }
 
 cudaError_t launch_combine(const CombineParams &p, int num_sms, cudaStream_t s)
@@ -361,8 +377,7 @@ cudaError_t launch_combine(const CombineParams &p, int num_sms, cudaStream_t s)
     default: {
         const int64_t units = static_cast<int64_t>(p.T) * ((p.N / 8 + 31) / 32);
         const int b = blocks_for(combine_kernel_any, num_sms, (units + 7) / 8);
-        combine_kernel_any<<<b, kCombineThreads, 0, s>>>(p);
-        return cudaGetLastError();
+        return launch_with(combine_kernel_any, b, p, s);
     }
     }
 }

@@ -436,6 +436,9 @@ __global__ void __launch_bounds__(224 + 32 * SEND, 1)
     }
 
     // --------------------------------------------------------------- teardown
+    // a combine launched behind this kernel may start now: it reads nothing before
+    // acquiring the flags (or count words) this kernel releases
+    griddep_launch_dependents();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

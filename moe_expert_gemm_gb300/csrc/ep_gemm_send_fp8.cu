@@ -356,6 +356,9 @@ __global__ void __launch_bounds__(352, 1)
             raise_abort(p.status, abort_flag);
     }
 
+    // a combine launched behind this kernel may start now: it reads nothing before
+    // acquiring the flags (or count words) this kernel releases
+    griddep_launch_dependents();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

@@ -336,6 +336,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
         __syncwarp();
     }
 
+    // a combine launched behind this kernel may start now: it reads nothing before
+    // acquiring the flags (or count words) this kernel releases
+    griddep_launch_dependents();
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();  // no MMA of the pair is still writing either CTA's TMEM

@@ -432,6 +432,14 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t *bar, uint16_t mask)
         : "memory");
 }
 
+// Programmatic dependent launch: this thread's part of the grid is done with the
+// work a dependent kernel may overlap; the dependent grid can start once every
+// thread block has signalled (or exited).
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // SiLU(x) = x / (1 + e^-x) in fp32 (expf of the CUDA math library).
 __device__ __forceinline__ float silu_f32(float x)
 {

@@ -253,16 +253,22 @@ class EpSystem:
         torch.cuda.synchronize()
         return decode_trace(buf.cpu().numpy().view(np.uint64), n_sm, records)
 
-    def combine_args(self, rank: int, epoch: int, gates=None, out=None) -> ep_combine_args:
+    def combine_args(self, rank: int, epoch: int, gates=None, out=None,
+                     overlap: bool = False) -> ep_combine_args:
         g = self.gates[rank] if gates is None else gates
         o = self.out[rank] if out is None else out
         return ep_combine_args(ptr(self.recv[rank]), ptr(self.counts[rank]), ptr(g), ptr(o),
                                epoch, self.timeout_ns,
                                self.status.data_ptr() + 4 * STATUS_COMBINE,
-                               ptr(self.topk[rank]) if self.topk is not None else 0)
+                               ptr(self.topk[rank]) if self.topk is not None else 0,
+                               1 if overlap else 0)
 
-    def combine(self, rank: int, epoch: int, stream=None, gates=None, out=None):
-        ep_combine_reduce(self.cfg(rank), self.combine_args(rank, epoch, gates, out), stream)
+    def combine(self, rank: int, epoch: int, stream=None, gates=None, out=None,
+                overlap: bool = False):
+        """``overlap``: may start while the fused send before it on the stream is still
+        finishing (programmatic dependent launch)."""
+        ep_combine_reduce(self.cfg(rank), self.combine_args(rank, epoch, gates, out, overlap),
+                          stream)
 
     def publish_peer_flags(self, rank: int, epoch: int):
         """Stand-in for the other ranks finishing on their own GPUs: write the flag

@@ -158,7 +158,7 @@ def test_fp8_has_no_dedicated_send_warps(lib):
 def test_per_expert_combine_needs_the_routing(lib):
     """In the per-expert mode the combine waits per token for the token's experts."""
     cfg = _cfg(signal_mode=ep.EP_SIGNAL_PER_EXPERT)
-    a = ep.ep_combine_args(0x1000000, 0x2000000, 0x3000000, 0x4000000, 1, 0, 0x5000000, 0)
+    a = ep.ep_combine_args(0x1000000, 0x2000000, 0x3000000, 0x4000000, 1, 0, 0x5000000, 0, 0)
     assert lib.ep_combine_reduce(ctypes.byref(cfg), ctypes.byref(a), None) == \
         ep.EP_ERR_INVALID_ARG
 

@@ -371,3 +371,35 @@ def test_per_expert_tokens_of_finished_ranks_are_combined_while_one_rank_is_miss
         assert (out[waits] == 0).all()
         assert combine_rel_err(out[~waits], ref["out_exact"][d][~waits],
                                ref["rows_exact"][d][~waits], routing.gates[d][~waits]) <= TOL["bf16"]
+
+
+OVERLAP_CASES = [
+    ("tiny", WORKLOADS["tiny"], 0),
+    ("qwen_shape_small", EDGE[8][1], 0),
+    ("pair_shape", Workload("ov_pair", 4, 3, 2, 400, 320, 512, "bf16", "zipf", "softmax_sel", 68),
+     0),
+    ("fp8_small", EDGE[10][1], 0),
+    ("tiny_per_expert", WORKLOADS["tiny"], 1),
+]
+
+
+@pytest.mark.parametrize("name,w,signal_mode", OVERLAP_CASES, ids=[c[0] for c in OVERLAP_CASES])
+def test_combine_overlapping_the_fused_send(name, w, signal_mode):
+    """The combine launched as a programmatic dependent of the destination's own
+    fused send (the last producer to run) starts before that send has ended; its
+    rows are ordered by the flags (or count words) it acquires, so the outputs
+    still match the oracle."""
+    routing, values = make_inputs(w)
+    s = build_system(w, routing, values, signal_mode=signal_mode)
+    for d in range(w.n_ranks):
+        for r in range(w.n_ranks):
+            if r != d:
+                s.send(r, epoch=10 + d)
+        s.send(d, epoch=10 + d)  # d's own send, then its combine right behind it
+        s.combine(d, epoch=10 + d, overlap=True)
+        torch.cuda.synchronize()
+        assert (s.status_words() == 0).all(), (d, s.status_words())
+        ref = full_pipeline(w, routing, values, epoch=10 + d, per_expert=bool(signal_mode))
+        out = s.out[d].view(torch.int16).cpu().numpy().view(np.uint16)
+        assert combine_rel_err(out, ref["out_exact"][d], ref["rows_exact"][d],
+                               routing.gates[d]) <= TOL[w.dtype], d
