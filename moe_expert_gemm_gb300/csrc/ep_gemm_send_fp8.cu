@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(352, 1)
         mbar_init(mma_done, 1);
         fence_mbar_init();
     }
-    sink_prologue(p, sh);
+    // the allocation and the descriptor prefetches overlap the prologue's loads
     if (warp == 1) {
         __syncwarp();
         tmem_alloc(&sh->tmem_slot, L::kTmemCols);
@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(352, 1)
         tma_prefetch_map(&tmap_a);
         tma_prefetch_map(&tmap_b);
     }
+    sink_prologue(p, sh);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

@@ -90,7 +90,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
         mbar_init(mma_done, 1);
         fence_mbar_init();
     }
-    sink_prologue(p, sh, L::kTileRows);
+    // the allocation and the descriptor prefetches overlap the prologue's loads
     if (warp == 1) {
         __syncwarp();
         tmem_alloc_pair(&sh->tmem_slot, L::kTmemCols);
@@ -100,6 +100,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
         tma_prefetch_map(&tmap_a);
         tma_prefetch_map(&tmap_b);
     }
+    sink_prologue(p, sh, L::kTileRows);
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();  // the peer's barriers exist before anyone signals them

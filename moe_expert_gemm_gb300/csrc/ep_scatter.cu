@@ -66,14 +66,15 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterP
         atomicOr(p.status, EP_STATUS_BOUNDS);
 
     // every block releases its rows (gpu scope) through the block counter; the last
-    // one acquires them all and signals every expert towards every destination
+    // one acquires them all (gpu scope) and signals every expert towards every
+    // destination behind system-scope releases, which carry the rows cumulatively
     __shared__ int s_last;
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
         const bool last = atomicAdd(p.block_counter, 1) == static_cast<int>(gridDim.x) - 1;
         if (last)
-            fence_acq_rel_sys();
+            fence_acq_rel_gpu();
         s_last = last;
     }
     __syncthreads();

@@ -43,14 +43,17 @@ __device__ __forceinline__ void raise_abort(uint32_t *status, volatile int *abor
 // call, waits on as few fences as possible:
 //  1. store_counts: the plain progress stores of expert e's count words, one per
 //     destination (values from shared memory, so no load sits between them);
-//  2. the caller's system-scope acquire-release fence: it acquires the expert's
-//     other tiles (whose rows the other blocks released before their tile-counter
-//     increments) and releases every row and count word of the expert to the peers;
+//  2. the caller's gpu-scope acquire-release fence: it acquires the expert's other
+//     tiles (whose rows the other blocks released before their tile-counter
+//     increments) and releases every row and count word of the expert into the
+//     election counters' modification order;
 //  3. elect_and_publish: the increments of the per-destination election counters
-//     (this GPU's memory, updated only by this GPU's blocks, so gpu-scope RMWs);
-//     the block that makes a counter reach E_l has acquired every other expert's
-//     release through that RMW chain, takes one more system-scope fence, re-arms
-//     the counter and publishes the rank flag.
+//     (this GPU's memory, updated only by this GPU's blocks, so gpu-scope RMWs,
+//     made acquire-release by the fences around them); the block that makes a
+//     counter reach E_l has acquired every other expert's release through that RMW
+//     chain, and its one system-scope fence is the single system-scope release that
+//     carries the whole rank (cumulatively) to the peers with the rank flag. It
+//     re-arms the counter and publishes the flag.
 __device__ __forceinline__ void store_counts(const SendParams &p, const SinkShared *sh, int e)
 {
     const int R = p.n_ranks;
@@ -171,27 +174,59 @@ __device__ __forceinline__ void sink_prologue(const SendParams &p, SinkShared *s
         sh->q_done = 0;
         sh->abort_flag = 0;
     }
-    for (int e = threadIdx.x; e <= El; e += blockDim.x)
-        sh->eoff[e] = __ldg(p.expert_offsets + e);
-    if (p.sink_enabled && El * p.n_ranks <= kCountCache)
-        for (int i = threadIdx.x; i < El * p.n_ranks; i += blockDim.x)
-            sh->counts[i] = __ldg(p.send_counts + i);
+    // one pass issues both loads of a thread before either store
+    const int n_cnt = p.sink_enabled && El * p.n_ranks <= kCountCache ? El * p.n_ranks : 0;
+    const int n_all = n_cnt > El + 1 ? n_cnt : El + 1;
+    for (int i = threadIdx.x; i < n_all; i += blockDim.x) {
+        const int eo = i <= El ? __ldg(p.expert_offsets + i) : 0;
+        const int cn = i < n_cnt ? __ldg(p.send_counts + i) : 0;
+        if (i <= El)
+            sh->eoff[i] = eo;
+        if (i < n_cnt)
+            sh->counts[i] = cn;
+    }
     __syncthreads();
-    if (threadIdx.x == 32) {
-        int prev = 0;
-        for (int e = 0; e <= El; ++e) {
-            int v = sh->eoff[e];
-            v = v < prev ? prev : v;
-            v = v > p.max_rows ? static_cast<int>(p.max_rows) : v;
-            sh->eoff[e] = v;
-            prev = v;
+    if ((threadIdx.x >> 5) == 2) {
+        // one warp, 32 experts at a time. Made monotone and clamped, the offsets are
+        // min(max(0, raw_0 .. raw_e), max_rows): a prefix maximum, then the clamp.
+        const int lane = threadIdx.x & 31;
+        const int max_rows = static_cast<int>(p.max_rows);
+        int carry = 0;
+        for (int base = 0; base <= El; base += 32) {
+            const int e = base + lane;
+            int m = e <= El ? sh->eoff[e] : 0;
+            m = m > carry ? m : carry;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, m, d);
+                if (lane >= d)
+                    m = o > m ? o : m;
+            }
+            carry = __shfl_sync(0xffffffffu, m, 31);
+            if (e <= El)
+                sh->eoff[e] = m < max_rows ? m : max_rows;
         }
+        __syncwarp();
+        // tile table: exclusive prefix sum of the experts' tile counts
         int acc = 0;
-        for (int e = 0; e < El; ++e) {
-            sh->tile_start[e] = acc;
-            acc += (sh->eoff[e + 1] - sh->eoff[e] + tile_rows - 1) / tile_rows * p.n_blocks;
+        for (int base = 0; base < El; base += 32) {
+            const int e = base + lane;
+            const int t = e < El
+                              ? (sh->eoff[e + 1] - sh->eoff[e] + tile_rows - 1) / tile_rows * p.n_blocks
+                              : 0;
+            int incl = t;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d)
+                    incl += o;
+            }
+            if (e < El)
+                sh->tile_start[e] = acc + incl - t;
+            acc += __shfl_sync(0xffffffffu, incl, 31);
         }
-        sh->tile_start[El] = acc;
+        if (lane == 0)
+            sh->tile_start[El] = acc;
     }
     __syncthreads();
 }
@@ -278,7 +313,10 @@ static __device__ void completion_loop(const SendParams &p, SinkShared *sh)
             }
         }
         if (any_empty) {
-            fence_acq_rel_sys();
+            if (per_expert)
+                fence_acq_rel_sys();
+            else
+                fence_acq_rel_gpu();
             for (int e = 0; e < p.El; ++e) {
                 if (sh->eoff[e + 1] == sh->eoff[e]) {
                     if (per_expert)
@@ -311,12 +349,17 @@ static __device__ void completion_loop(const SendParams &p, SinkShared *sh)
                 any |= last[j];
             }
             if (any) {
-                if (!per_expert)
+                // acquire the experts' other tiles; release their rows (and counts):
+                // per expert, to the peers directly (each count word is a system-scope
+                // release); with the rank flag, to the election on this GPU
+                if (per_expert) {
+                    fence_acq_rel_sys();
+                } else {
                     for (int j = 0; j < n; ++j)
                         if (last[j])
                             store_counts(p, sh, ent[j].x);
-                // acquire the experts' other tiles; release their rows (and counts)
-                fence_acq_rel_sys();
+                    fence_acq_rel_gpu();
+                }
             }
             for (int j = 0; j < n; ++j) {
                 if (last[j]) {

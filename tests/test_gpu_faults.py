@@ -65,3 +65,49 @@ def test_out_of_range_destination_is_skipped_and_reported():
         written = bool((row != -1).any())
         assert written == (m != bad_row), m
     assert dst >= 0
+
+
+@pytest.mark.parametrize("kind", ["end_past_rows", "non_monotone"])
+def test_malformed_expert_offsets_are_clamped(kind):
+    """A corrupted plan's expert row ranges are made monotone and clamped to the rows
+    of A: expert e runs over [o_e, o_{e+1}) with o_e = min(max(0, raw_0 .. raw_e),
+    max_rows). Rows that then lie outside every destination segment of their expert
+    are skipped with EP_STATUS_BOUNDS; every other row arrives as in an intact call,
+    every count word and the rank flag are published, and nothing waits out."""
+    w = WORKLOADS["tiny"]
+    routing, values = make_inputs(w)
+    r = 1
+    good = build_system(w, routing, values)
+    good.send(r, epoch=1)
+    s = build_system(w, routing, values)
+    s.set_operands(r, values[r]["A"], values[r]["W"], pad_rows=64)  # rows past m_total
+    eo = s.plans[r]["expert_offsets"]
+    raw = eo.cpu().numpy().copy()
+    max_rows = int(s.send_args(r, 1).max_rows)
+    assert max_rows > raw[-1] + 5
+    if kind == "end_past_rows":
+        raw[-1] = max_rows + 1000  # rows [m_total, max_rows) join the last expert
+        skipped_experts = set()
+    else:
+        raw[1] = raw[2] + 5  # expert 0 would end past expert 1, which becomes empty
+        skipped_experts = {1}
+    eo.copy_(torch.from_numpy(raw))
+    s.send(r, epoch=1)
+    torch.cuda.synchronize()
+    st = s.status_words()
+    assert st[1] & ep.EP_STATUS_BOUNDS
+    assert not st[1] & ep.EP_STATUS_TIMEOUT
+    for d in range(w.n_ranks):
+        np.testing.assert_array_equal(s.counts[d].cpu().numpy(), good.counts[d].cpu().numpy())
+    pl = good.plan_host(r)
+    seg = pl["seg_offsets"]
+    for m in range(pl["m_total"]):
+        e = int(np.searchsorted(pl["expert_offsets"], m, side="right") - 1)
+        d = int(np.searchsorted(seg[e], m, side="right") - 1)
+        t, j = (int(x) for x in pl["src_info"][m])
+        sl = slice((t * w.top_k + j) * w.N, (t * w.top_k + j + 1) * w.N)
+        got = s.recv[d].view(torch.int16)[sl].cpu()
+        if e in skipped_experts:
+            assert bool((got == -1).all()), m
+        else:
+            assert torch.equal(got, good.recv[d].view(torch.int16)[sl].cpu()), m

@@ -90,6 +90,11 @@ EDGE = [
                                "softmax_sel", 47), "empty"),
     ("qwen_shape_small", Workload("qwen_small", 8, 16, 8, 48, 1536, 4096, "bf16", "zipf",
                                   "softmax_sel", 48), "random"),
+    # more than 32 local experts: the kernels' tile table spans several warp-wide scans
+    ("many_local_experts", Workload("many_el", 2, 48, 4, 64, 128, 128, "bf16", "uniform",
+                                    "softmax_sel", 73), "random"),
+    ("many_local_experts_pairs", Workload("many_el_pair", 1, 40, 8, 1300, 128, 256, "bf16",
+                                          "uniform", "softmax_sel", 74), "random"),
     # a top_k with no specialised combine (3)
     ("topk3", Workload("topk3", 4, 2, 3, 40, 128, 256, "bf16", "uniform", "softmax_sel", 55),
      "random"),
