@@ -14,7 +14,8 @@
 // partial buffers the MMA -> promotion -> MMA hand-off is on the critical path of
 // every K block, and across a CTA pair that round trip doubles.
 //  warp 0     TMA: A box 128 (K bytes) x 128 rows, W box 128 x BN, 128-byte swizzle;
-//             one stage is exactly one scale block (4 stages; 6 for BN 128).
+//             one stage is exactly one scale block (3 stages; 5 for BN 128: the
+//             shared memory left holds the output tile).
 //  warp 1     TMEM (512 columns = 512/BN fp32 partial buffers of 128 x BN) and the MMA:
 //             tcgen05.mma kind::f8f6f4, e4m3 x e4m3, M 128, N BN, K 32 per instruction;
 //             one partial per K block, buffers in rotation.
@@ -22,8 +23,12 @@
 //  warps 3-10 promotion + epilogue: warp w reads TMEM lane quarter w % 4 and column
 //             half (w - 3) / 4; each thread keeps its row's BN/2 fp32 accumulators
 //             (as pairs, updated with paired FMAs), adds sa[m, kb] * sw[e, n/128, kb] *
-//             partial per K block, then rounds to bf16 and sends the row in 64-byte
-//             pieces (4 lanes per row).
+//             partial per K block, then rounds to bf16 into a shared-memory tile
+//             buffer and sends its BN/2 columns with one bulk copy (the row's bytes
+//             are contiguous at the destination). The copies run on the TMA engine
+//             while the warps promote the next tile; a tile goes to the completion
+//             warp once its copies have completed (at the next tile's epilogue, or
+//             after the last tile), so the rows it signals are written.
 #include <cuda_bf16.h>
 
 #include "ep_internal.h"
@@ -44,22 +49,34 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
         : "memory");
 }
 
+// Tile number i of this block (expert e), whose rows have all been written, goes to
+// the completion warp.
+__device__ __forceinline__ bool push_written_tile(const SendParams &p, SinkShared *sh,
+                                                  uint64_t *trace, int e, int i)
+{
+    const int rec = (trace && i < p.trace_records) ? i : -1;
+    if (rec >= 0)
+        trace[2 + 4 * rec + 2] = globaltimer_ns();
+    const int tiles_e = (sh->eoff[e + 1] - sh->eoff[e] + BM - 1) / BM * p.n_blocks;
+    return push_tile_done(p, sh, e, rec, tiles_e);
+}
+
 template <int BN_>
 struct Fp8Layout {
     static constexpr int BN = BN_;
-    static constexpr int STAGES = BN == 128 ? 6 : 4;
+    static constexpr int STAGES = BN == 128 ? 5 : 3;
     static constexpr int kBufs = 512 / BN;    // fp32 partial buffers that fit in TMEM
     static constexpr int kHalfCols = BN / 2;  // columns per promotion warp
     static constexpr int kABytes = BM * kRowBytesK;  // 128 rows x 128 e4m3
     static constexpr int kBBytes = BN * kRowBytesK;  // BN rows x 128 e4m3
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kPromoWarps = 8;
-    static constexpr int kStgRow = 80;                 // 64 data bytes + 16 pad
-    static constexpr int kWarpStaging = 32 * kStgRow;  // 32 rows x 32 bf16 columns
+    static constexpr int kTilePitch = BN * 2 + 16;  // a bf16 output row + 16 bytes: rows
+                                                     // of a warp's stores hit all banks
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + STAGES * kABytes;
-    static constexpr int kOffStaging = kOffB + STAGES * kBBytes;
-    static constexpr int kOffBars = kOffStaging + kPromoWarps * kWarpStaging;
+    static constexpr int kOffTile = kOffB + STAGES * kBBytes;
+    static constexpr int kOffBars = kOffTile + BM * kTilePitch;
     static constexpr int kNumBars = 2 * STAGES + 2 * kBufs + 1;  // full, empty, pfull, pfree, done
     static constexpr int kOffSink = (kOffBars + kNumBars * 8 + 15) / 16 * 16;
     static constexpr int kEnd = kOffSink + static_cast<int>(sizeof(SinkShared));
@@ -221,7 +238,10 @@ __global__ void __launch_bounds__(352, 1)
         const int q = warp & 3;            // TMEM lane quarter
         const int half = (warp - 3) >> 2;  // column half of the tile
         const int ptid = threadIdx.x - 96;  // 0..255
-        const uint32_t stg = smem_u32(smem + L::kOffStaging + (warp - 3) * L::kWarpStaging);
+        // this thread's row of the tile buffer (its HC columns)
+        const uint32_t trow = smem_u32(smem + L::kOffTile) + (q * 32 + lane) * L::kTilePitch +
+                              half * HC * 2;
+        int pend_e = -1;  // expert of the previous tile, whose copies may be in flight
         const int row = q * 32 + lane;
         const int n_scale_blocks = p.N / 128;
         uint64_t *trace = ptid == 0 ? trace_block(p) : nullptr;
@@ -302,50 +322,41 @@ __global__ void __launch_bounds__(352, 1)
                 rec[1] = globaltimer_ns();
             }
 
-            // bf16 rows, 32 columns at a time: stage, then 4 lanes per row send 64 bytes
+            // the previous tile's copies have read the buffer and written their rows:
+            // hand that tile to the completion warp
+            bulk_wait_all();
+            fence_proxy_async_global();
+            named_bar_sync(1, 256);
+            if (ptid == 0 && pend_e >= 0 && p.sink_enabled)
+                push_ok = push_written_tile(p, sh, trace, pend_e, i - 1) && push_ok;
+            // this thread's row in bf16 into the buffer, then one bulk copy of it
 #pragma unroll
-            for (int c4 = 0; c4 < HC / 32; ++c4) {
+            for (int ch = 0; ch < HC / 8; ++ch) {
+                uint32_t w[4];
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const uint64_t a2 = acc[c4 * 16 + ch * 4 + h];
-                        __nv_bfloat162 b = __float22bfloat162_rn(
-                            make_float2(__uint_as_float(static_cast<uint32_t>(a2)),
-                                        __uint_as_float(static_cast<uint32_t>(a2 >> 32))));
-                        w[h] = *reinterpret_cast<uint32_t *>(&b);
-                    }
-                    st_shared_v4(stg + lane * L::kStgRow + ch * 16,
-                                 make_uint4(w[0], w[1], w[2], w[3]));
+                for (int h = 0; h < 4; ++h) {
+                    const uint64_t a2 = acc[ch * 4 + h];
+                    __nv_bfloat162 b = __float22bfloat162_rn(
+                        make_float2(__uint_as_float(static_cast<uint32_t>(a2)),
+                                    __uint_as_float(static_cast<uint32_t>(a2 >> 32))));
+                    w[h] = *reinterpret_cast<uint32_t *>(&b);
                 }
-                __syncwarp();
-                const int col_byte = (c.nb * BN + half * HC + c4 * 32) * 2;
-#pragma unroll
-                for (int it = 0; it < 4; ++it) {
-                    const int r = it * 8 + (lane >> 2);
-                    const int ch = lane & 3;
-                    const unsigned long long base = __shfl_sync(
-                        0xffffffffu, reinterpret_cast<unsigned long long>(row_base), r);
-                    const uint4 val = ld_shared_v4(stg + r * L::kStgRow + ch * 16);
-                    if (base != 0ull)
-                        st_global_v4(reinterpret_cast<uint8_t *>(base) + col_byte + ch * 16, val);
-                }
-                __syncwarp();
+                st_shared_v4(trow + ch * 16, make_uint4(w[0], w[1], w[2], w[3]));
             }
-
-            if (p.sink_enabled) {
-                named_bar_sync(1, 256);
-                if (ptid == 0) {
-                    if (rec)
-                        rec[2] = globaltimer_ns();
-                    const int tiles_e = (c.m_end - sh->eoff[c.e] + BM - 1) / BM * p.n_blocks;
-                    push_ok = push_tile_done(p, sh, c.e, rec ? i : -1, tiles_e);
-                }
-            } else if (rec) {
+            fence_proxy_async_shared();
+            if (row_base != nullptr)
+                bulk_store(row_base + (c.nb * BN + half * HC) * 2, trow, HC * 2);
+            bulk_commit();
+            pend_e = c.e;
+            if (!p.sink_enabled && rec)
                 rec[2] = rec[3] = globaltimer_ns();
-            }
         }
+        // the last tile's copies
+        bulk_wait_all();
+        fence_proxy_async_global();
+        named_bar_sync(1, 256);
+        if (ptid == 0 && pend_e >= 0 && p.sink_enabled && ok)
+            push_ok = push_written_tile(p, sh, trace, pend_e, i - 1) && push_ok;
         if (ptid == 0) {
             if (trace)
                 trace[0] = static_cast<uint64_t>(i);

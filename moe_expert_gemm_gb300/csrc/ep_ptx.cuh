@@ -120,6 +120,40 @@ __device__ __forceinline__ uint64_t policy_evict_first()
     return p;
 }
 
+// Untiled bulk copy from shared to global memory on the TMA engine (both addresses
+// 16-byte aligned, bytes a multiple of 16), tracked per thread in bulk groups.
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Every bulk group this thread committed has completed: its shared memory was read
+// and its global writes are performed.
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// This thread's generic-proxy shared-memory writes before async-proxy reads of them.
+__device__ __forceinline__ void fence_proxy_async_shared()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Async-proxy global writes (completed bulk copies) before this thread's later
+// generic-proxy accesses and the releases that follow them.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ------------------------------------------------------------------- tcgen05
 
 // Whole warp: allocate `ncols` TMEM columns (power of two >= 32); the base
