@@ -57,6 +57,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixtral_prefill")
+    ap.add_argument("--rank", default="0",
+                    help="logical rank timed at N=1 (replicas start from it): an index, or "
+                         "'max' for the rank that receives the most rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -240,9 +243,9 @@ def cpu_sample(w, routing, values, dst: int, target_s: float, plans: dict):
 # region is bracketed by barriers, the step time is the maximum over processes
 # and the reported value is the whole job's tokens over that time.
 
-def replica_rank(rank: int, n_ranks: int) -> int:
-    """The logical rank a process plays."""
-    return rank % n_ranks
+def replica_rank(rank: int, n_ranks: int, first: int = 0) -> int:
+    """The logical rank a process plays (process 0 plays `first`)."""
+    return (first + rank) % n_ranks
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
@@ -270,6 +273,9 @@ def run_reference(args, rank, world):
     w = WORKLOADS[args.workload]
     routing = make_routing(w)
     rows = rows_per_rank(w, routing.topk_ids)
+    q = int(np.argmax(rows)) if args.rank == "max" else int(args.rank)
+    if not 0 <= q < w.n_ranks:
+        raise SystemExit(f"--rank must name a logical rank below {w.n_ranks}")
     values = [make_rank_values(w, r, int(rows[r])) for r in range(w.n_ranks)]
     plans = {r: oracle.plan(w.n_ranks, w.n_local_experts, w.top_k, routing.topk_ids, r)
              for r in range(w.n_ranks)}
@@ -278,7 +284,7 @@ def run_reference(args, rank, world):
     rng = np.random.default_rng(7)
     probe = min(w.tokens, 16)
     t0 = time.perf_counter()
-    sampled_pipeline(w, routing, lambda r: values[r], 0, rng.permutation(w.tokens)[:probe],
+    sampled_pipeline(w, routing, lambda r: values[r], q, rng.permutation(w.tokens)[:probe],
                      plans=plans)
     per_tok = max((time.perf_counter() - t0) / probe, 1e-9)
     n = int(min(w.tokens, max(1, budget / per_tok)))
@@ -286,13 +292,13 @@ def run_reference(args, rank, world):
     for i in range(args.warmup + args.steps):
         toks = np.sort(rng.permutation(w.tokens)[:n])
         t0 = time.perf_counter()
-        sampled_pipeline(w, routing, lambda r: values[r], 0, toks, plans=plans)
+        sampled_pipeline(w, routing, lambda r: values[r], q, toks, plans=plans)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     step_s = sum(times) / len(times)
     value = n / step_s
     cores = oracle.default_threads()
-    sample = (f"each step: {n} of rank 0's {w.tokens} tokens, their {w.top_k} rows each "
+    sample = (f"each step: {n} of rank {q}'s {w.tokens} tokens, their {w.top_k} rows each "
               f"(GEMM from every producer rank) and their combine")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -300,7 +306,7 @@ def run_reference(args, rank, world):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "n_ranks": w.n_ranks,
                        "n_local_experts": w.n_local_experts, "top_k": w.top_k,
-                       "tokens_per_rank": w.tokens, "K": w.K, "N": w.N, "my_rank": 0},
+                       "tokens_per_rank": w.tokens, "K": w.K, "N": w.N, "my_rank": q},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -335,9 +341,12 @@ def main():
     if args.tokens:
         import dataclasses
         w = dataclasses.replace(w, tokens=args.tokens, name=f"{w.name}@T{args.tokens}")
-    q = replica_rank(rank, w.n_ranks)  # the logical rank this process plays
     routing = make_routing(w)
     rows = rows_per_rank(w, routing.topk_ids)
+    first = int(np.argmax(rows)) if args.rank == "max" else int(args.rank)
+    if not 0 <= first < w.n_ranks:
+        raise SystemExit(f"--rank must name a logical rank below {w.n_ranks}")
+    q = replica_rank(rank, w.n_ranks, first)  # the logical rank this process plays
     ranks = [q] if args.solo else list(range(w.n_ranks))
     layer = args.path == "layer"
     if layer and (w.dtype != "bf16" or args.solo):

@@ -68,4 +68,5 @@ def test_single_process_helpers():
     import bench
     assert bench.max_over_ranks(1.25, 1, "cpu") == 1.25
     assert bench.replica_rank(9, 8) == 1
+    assert bench.replica_rank(3, 8, first=6) == 1  # replicas start from the timed rank
     assert bench.job_tokens_per_s(1, 1000, 2.0) == 500_000.0
