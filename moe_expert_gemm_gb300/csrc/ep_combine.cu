@@ -13,10 +13,10 @@
 // once. R threads per block acquire the R source flags (bounded waits), then a warp
 // handles units of 256 contiguous columns of one token: 32 lanes x 16-byte loads of
 // each of the token's top_k rows, fp32 accumulation in slot order, one 16-byte
-// streaming store. A warp takes max(1, 8 / top_k) consecutive units at a time and
-// issues all their loads before accumulating, so each thread keeps about eight
-// 16-byte loads in flight. The grid is at most one wave of 8 blocks per SM with a
-// grid-stride loop.
+// streaming store. A warp takes several consecutive units at a time (8 / top_k;
+// for top_k >= 8 on large calls 16 / top_k) and issues all their loads before
+// accumulating, so each thread keeps 8-16 16-byte loads in flight. The grid is one
+// resident wave (four for the 16-load form) with a grid-stride loop.
 #include <cuda_bf16.h>
 
 #include "ep_internal.h"
@@ -25,7 +25,15 @@
 namespace ep {
 
 constexpr int kCombineThreads = 256;
-constexpr int kLoads = 8;  // 16-byte row loads a thread keeps in flight
+constexpr int kLoads = 8;  // 16-byte row loads a thread keeps in flight (at least)
+
+// Units a warp reduces at once for a compile-time top_k: about kLoads row loads per
+// thread in flight (one unit for run-time top_k).
+template <int K>
+constexpr int units_at_once()
+{
+    return K == 0 ? 1 : (K >= kLoads ? 1 : kLoads / K);
+}
 
 __device__ __forceinline__ void store_out(const CombineParams &p, int64_t t, int64_t v,
                                           const float (&acc)[8])
@@ -74,14 +82,13 @@ __device__ __forceinline__ bool acquire_source_flags(const CombineParams &p)
     return s_ok != 0;
 }
 
-// top_k known at compile time: a warp takes U = max(1, kLoads / K) consecutive units
-// and issues all U*K loads before accumulating any of them.
-template <int K>
+// top_k known at compile time: a warp takes U consecutive units and issues all U*K
+// loads before accumulating any of them.
+template <int K, int U>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p)
 {
     if (!acquire_source_flags(p))
         return;
-    constexpr int U = K >= kLoads ? 1 : kLoads / K;
     const int lane = threadIdx.x & 31;
     const int warps = kCombineThreads / 32;
     const int64_t vec_per_row = p.N / 8;  // 16-byte vectors of one output row
@@ -173,12 +180,12 @@ __device__ __forceinline__ bool token_arrived(const CombineParams &p, int64_t t,
 
 // EP_SIGNAL_PER_EXPERT consumer: every warp takes a contiguous range of (token,
 // 256-column unit) work items and, whenever its range enters a new token, acquires
-// that token's experts; then it reduces the token's units U = max(1, kLoads / K) at
-// a time, all U*K row loads issued before accumulating. A token whose experts have
+// that token's experts; then it reduces the token's units U at a time, all U*K row
+// loads issued before accumulating. A token whose experts have
 // all arrived is reduced whatever the other experts are doing; one whose expert
 // never arrives is left unwritten (EP_STATUS_TIMEOUT). K = 0: top_k known at run
 // time only.
-template <int K>
+template <int K, int U>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel_per_expert(const CombineParams p)
 {
     __shared__ int s_gave_up;
@@ -186,7 +193,6 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel_per_expert(con
         s_gave_up = 0;
     __syncthreads();
     volatile int *gave_up = &s_gave_up;
-    constexpr int U = K == 0 ? 1 : (K >= kLoads ? 1 : kLoads / K);
     const int k = K == 0 ? p.top_k : K;
     const int lane = threadIdx.x & 31;
     const int64_t vec_per_row = p.N / 8;
@@ -317,7 +323,7 @@ static cudaError_t launch_with(void (*kern)(CombineParams), int blocks, const Co
 }
 
 template <typename Kern>
-static int blocks_for(Kern kern, int num_sms, int64_t work_blocks)
+static int blocks_for(Kern kern, int num_sms, int64_t work_blocks, int waves = 1)
 {
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCombineThreads, 0) !=
@@ -326,27 +332,62 @@ static int blocks_for(Kern kern, int num_sms, int64_t work_blocks)
         (void)cudaGetLastError();
         per_sm = 1;
     }
-    const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;  // one resident wave
+    const int64_t cap = static_cast<int64_t>(waves) * num_sms * per_sm;  // resident waves
     int64_t b = work_blocks < cap ? work_blocks : cap;
     return static_cast<int>(b < 1 ? 1 : b);
+}
+
+// Per call, the kernel form: U = units_at_once<K>(), or twice that for top_k >= kLoads
+// when every resident warp would get at least kWideUnits units (16 loads in flight
+// per thread: the fp8 prefill combine 177 -> 162 us, 0.88 -> 0.95 of the copy
+// bandwidth; on smaller calls the fewer, longer warps cost more at the tail). The
+// wide form's grid is up to four resident waves: a combine launched behind the send
+// starts on SMs as the send's blocks leave, and smaller blocks spread the work over
+// the SMs that free up last (the narrow form keeps one wave: its blocks are short,
+// and each extra block acquires the flags again).
+constexpr int64_t kWideUnits = 32;
+
+template <int K>
+static cudaError_t launch_form(const CombineParams &p, int num_sms, cudaStream_t s,
+                               void (*narrow)(CombineParams), void (*wide)(CombineParams))
+{
+    constexpr int U = units_at_once<K>();
+    const int64_t units = static_cast<int64_t>(p.T) * ((p.N / 8 + 31) / 32);
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, narrow, kCombineThreads, 0) !=
+            cudaSuccess ||
+        per_sm < 1) {
+        (void)cudaGetLastError();
+        per_sm = 1;
+    }
+    const int64_t resident_warps = static_cast<int64_t>(num_sms) * per_sm * (kCombineThreads / 32);
+    if (K >= kLoads && wide != nullptr && units >= kWideUnits * resident_warps) {
+        const int b = blocks_for(wide, num_sms, (units + 16 * U - 1) / (16 * U), 4);
+        return launch_with(wide, b, p, s);
+    }
+    const int b = blocks_for(narrow, num_sms, (units + 8 * U - 1) / (8 * U));
+    return launch_with(narrow, b, p, s);
 }
 
 template <int K>
 static cudaError_t launch_k(const CombineParams &p, int num_sms, cudaStream_t s)
 {
-    constexpr int U = K >= kLoads ? 1 : kLoads / K;
-    const int64_t units = static_cast<int64_t>(p.T) * ((p.N / 8 + 31) / 32);
-    const int b = blocks_for(combine_kernel<K>, num_sms, (units + 8 * U - 1) / (8 * U));
-    return launch_with(combine_kernel<K>, b, p, s);
+    constexpr int U = units_at_once<K>();
+    if constexpr (K >= kLoads)
+        return launch_form<K>(p, num_sms, s, combine_kernel<K, U>, combine_kernel<K, 2 * U>);
+    else
+        return launch_form<K>(p, num_sms, s, combine_kernel<K, U>, nullptr);
 }
 
 template <int K>
 static cudaError_t launch_per_expert(const CombineParams &p, int num_sms, cudaStream_t s)
 {
-    constexpr int U = K == 0 ? 1 : (K >= kLoads ? 1 : kLoads / K);
-    const int64_t units = static_cast<int64_t>(p.T) * ((p.N / 8 + 31) / 32);
-    const int b = blocks_for(combine_kernel_per_expert<K>, num_sms, (units + 8 * U - 1) / (8 * U));
-    return launch_with(combine_kernel_per_expert<K>, b, p, s);
+    constexpr int U = units_at_once<K>();
+    if constexpr (K >= kLoads)
+        return launch_form<K>(p, num_sms, s, combine_kernel_per_expert<K, U>,
+                              combine_kernel_per_expert<K, 2 * U>);
+    else
+        return launch_form<K>(p, num_sms, s, combine_kernel_per_expert<K, U>, nullptr);
 }
 
 cudaError_t launch_combine(const CombineParams &p, int num_sms, cudaStream_t s)
