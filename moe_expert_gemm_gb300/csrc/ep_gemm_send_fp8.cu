@@ -81,7 +81,8 @@ struct Fp8Layout {
     static constexpr int kOffSink = (kOffBars + kNumBars * 8 + 15) / 16 * 16;
     static constexpr int kEnd = kOffSink + static_cast<int>(sizeof(SinkShared));
     static constexpr int kSmemBytes = kEnd + 1024;
-    static constexpr uint32_t kTmemCols = 2 * BN;
+    static constexpr uint32_t kTmemCols = kBufs * BN;  // all 512 columns
+    static_assert(kBufs * BN == 512, "the partial buffers fill the allocation");
     static constexpr int kThreads = 32 * (3 + kPromoWarps);
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };

@@ -105,6 +105,9 @@ EDGE = [
                                 "sigmoid_sel", 52), "random"),
     ("fp8_dsv3_shape_small", Workload("fp8_dsv3_small", 8, 32, 8, 64, 2048, 7168, "fp8_1d2d",
                                       "uniform", "sigmoid_sel", 53), "random"),
+    # N % 256 = 128: the fp8 kernel's 128-column tiles (four partial buffers)
+    ("fp8_128_column_tiles", Workload("fp8_n384", 4, 2, 2, 80, 384, 384, "fp8_1d2d", "uniform",
+                                      "sigmoid_sel", 77), "random"),
 ]
 
 
