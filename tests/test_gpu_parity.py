@@ -111,6 +111,9 @@ EDGE = [
 ]
 
 
+_EDGE = {name: w for name, w, _ in EDGE}  # edge workloads by name
+
+
 @pytest.mark.parametrize("name,w,kind", EDGE, ids=[e[0] for e in EDGE])
 def test_edge_parity(name, w, kind):
     routing = make_routing(w)
@@ -301,10 +304,10 @@ def test_fp8_identity_weights_bit_exact(T):
 
 UNFUSED_CASES = [
     ("tiny", WORKLOADS["tiny"]),
-    ("hot_pair_ragged", EDGE[0][1]),
-    ("eight_ranks_one_expert", EDGE[5][1]),
+    ("hot_pair_ragged", _EDGE["hot_pair_ragged"]),
+    ("eight_ranks_one_expert", _EDGE["eight_ranks_one_expert"]),
     ("pair_shape", Workload("uf_pair", 4, 3, 2, 400, 320, 512, "bf16", "zipf", "softmax_sel", 66)),
-    ("fp8_small", EDGE[10][1]),
+    ("fp8_small", _EDGE["fp8_small"]),
 ]
 
 
@@ -329,12 +332,13 @@ def test_unfused_send_parity(name, w):
 
 PER_EXPERT_CASES = [
     ("tiny", WORKLOADS["tiny"], False),
-    ("empty_experts", EDGE[7][1], False),
-    ("eight_ranks_one_expert", EDGE[5][1], False),
-    ("topk3", EDGE[9][1], False),
+    ("empty_experts", _EDGE["empty_experts"], False),
+    ("eight_ranks_one_expert", _EDGE["eight_ranks_one_expert"], False),
+    ("topk3", _EDGE["topk3"], False),
     ("pair_shape", Workload("pe_pair", 4, 3, 2, 400, 320, 512, "bf16", "zipf", "softmax_sel", 67),
      False),
-    ("fp8_small", EDGE[10][1], False),
+    ("fp8_small", _EDGE["fp8_small"], False),
+    ("many_local_experts", _EDGE["many_local_experts"], False),
     ("tiny_unfused", WORKLOADS["tiny"], True),
 ]
 
@@ -383,10 +387,10 @@ def test_per_expert_tokens_of_finished_ranks_are_combined_while_one_rank_is_miss
 
 OVERLAP_CASES = [
     ("tiny", WORKLOADS["tiny"], 0),
-    ("qwen_shape_small", EDGE[8][1], 0),
+    ("qwen_shape_small", _EDGE["qwen_shape_small"], 0),
     ("pair_shape", Workload("ov_pair", 4, 3, 2, 400, 320, 512, "bf16", "zipf", "softmax_sel", 68),
      0),
-    ("fp8_small", EDGE[10][1], 0),
+    ("fp8_small", _EDGE["fp8_small"], 0),
     ("tiny_per_expert", WORKLOADS["tiny"], 1),
 ]
 
