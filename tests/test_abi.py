@@ -166,3 +166,37 @@ def test_per_expert_combine_needs_the_routing(lib):
 def test_strerror(lib):
     assert ep.ep_strerror(ep.EP_ERR_UNSUPPORTED) == "unsupported configuration"
     assert "timed out" in ep.ep_strerror(ep.EP_STATUS_TIMEOUT)
+
+
+def test_binding_structs_match_the_header(tmp_path):
+    """Every argument struct of the binding has the header's size and, field by field,
+    its offsets and sizes (a C program built from the header prints them)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = [ep.ep_config, ep.ep_plan_out, ep.ep_send_args, ep.ep_combine_args,
+               ep.ep_scatter_args, ep.ep_dispatch_args, ep.ep_swiglu_args]
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "moe_ep.h"', "int main(void) {"]
+    for cls in structs:
+        name = cls.__name__
+        lines.append(f'printf("{name} size %zu\\n", sizeof({name}));')
+        for field, _ in cls._fields_:
+            lines.append(f'printf("{name} {field} %zu %zu\\n", offsetof({name}, {field}), '
+                         f'sizeof((({name} *)0)->{field}));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True, capture_output=True)
+    got = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    want = []
+    for cls in structs:
+        name = cls.__name__
+        want.append(f"{name} size {ctypes.sizeof(cls)}")
+        for field, _ in cls._fields_:
+            d = getattr(cls, field)
+            want.append(f"{name} {field} {d.offset} {d.size}")
+    assert [g for g in got if g] == want
