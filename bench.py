@@ -410,7 +410,7 @@ def main():
     # the combine may start while the fused send finishes (its rows are ordered by the
     # flags it acquires, not by the kernel boundary); the per-kernel breakdown is taken
     # from separately timed steps with the two kernels serialised
-    overlap = not args.no_overlap and not unfused and not layer
+    overlap = not args.no_overlap and not unfused
 
     def one_step(evs=None, serial=False):
         e = epoch[0]
@@ -421,9 +421,10 @@ def main():
         if evs is not None:
             evs[0].record(stream)
         if layer:
-            s.layer_forward(q, e, stream, events=None if evs is None
-                            else [evs[4], evs[5], evs[6], evs[7]],
-                            fused_act=args.layer_act == "fused")
+            inner = evs is not None and (serial or not overlap)
+            s.layer_forward(q, e, stream, events=[evs[4], evs[5], evs[6], evs[7]] if inner
+                            else None, fused_act=args.layer_act == "fused",
+                            overlap=overlap and not serial)
         elif unfused:
             s.send(q, e, stream, p3_control=-1, C=C_local)
             if evs is not None:
@@ -633,7 +634,9 @@ def main():
                         "ep_combine_reduce": statistics.mean(comb_ms)}),
         "combine_gbs": comb_bytes / comb_s / 1e9,
         "roofline": roof,
-        "gpu_launches": (5 if layer else 3 if unfused else 2) * args.steps,
+        # dispatch, up/gate GEMM (+ ep_swiglu when separate), send, combine
+        "gpu_launches": ((4 if args.layer_act == "fused" else 5) if layer
+                         else 3 if unfused else 2) * args.steps,
         "clocks": clk,
     }
     if e2e is not None:

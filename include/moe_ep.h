@@ -202,6 +202,12 @@ int ep_plan(const ep_config *cfg, const int32_t *topk_ids, const ep_plan_out *ou
  *                    each records it.
  *   timeout_ns       limit of each bounded wait inside the kernel (0: 2 s).
  *   trace_records    records per thread block in `trace` (>= 1 when trace is set).
+ *   overlap_previous nonzero: launch as a programmatic dependent of the previous kernel
+ *                    on `stream`. The thread blocks then start while that kernel is
+ *                    still finishing and do their set-up (barriers, tensor memory,
+ *                    descriptor prefetch) meanwhile, and wait for its completion and
+ *                    memory before reading or writing any global memory, so the
+ *                    previous kernel may produce the plan or the operands.
  *   local_activation with p3_control < 0 only (else ignored): EP_ACT_NONE stores the
  *                    rows as they are; EP_ACT_SWIGLU makes the call the up/gate
  *                    projection of a gated MLP with the activation in its epilogue:
@@ -237,6 +243,7 @@ typedef struct {
     int64_t timeout_ns;
     int64_t trace_records;
     int32_t local_activation;
+    int32_t overlap_previous;
 } ep_send_args;
 
 /*

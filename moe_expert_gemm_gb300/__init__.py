@@ -58,7 +58,7 @@ class ep_send_args(ctypes.Structure):
                 ("atomic_counter", _vp), ("rank_completion_counter", _vp), ("epoch", _c_u64),
                 ("p3_control", _c_i32), ("C", _vp), ("status", _vp), ("trace", _vp),
                 ("timeout_ns", _c_i64), ("trace_records", _c_i64),
-                ("local_activation", _c_i32)]
+                ("local_activation", _c_i32), ("overlap_previous", _c_i32)]
 
 
 class ep_combine_args(ctypes.Structure):

@@ -292,6 +292,7 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     p.w_scales = a->w_scales;
     p.trace = a->trace;
     p.trace_records = a->trace ? static_cast<int>(a->trace_records) : 0;
+    p.overlap_previous = a->overlap_previous ? 1 : 0;
 
     // the plan lives on the device, so size the grid by the worst-case tile count
     const int64_t max_tiles = ((a->max_rows + ep::BM - 1) / ep::BM + El) * p.n_blocks;

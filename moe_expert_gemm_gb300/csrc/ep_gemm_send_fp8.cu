@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(352, 1)
         tma_prefetch_map(&tmap_a);
         tma_prefetch_map(&tmap_b);
     }
+    griddep_wait();  // from here on global memory may be what the previous kernel wrote
     sink_prologue(p, sh);
     tc_fence_before();
     __syncthreads();
@@ -390,8 +391,7 @@ static cudaError_t launch_fp8_bn(const CUtensorMap &ta, const CUtensorMap &tb,
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (err != cudaSuccess)
         return err;
-    kern<<<grid, L::kThreads, L::kSmemBytes, s>>>(ta, tb, p);
-    return cudaGetLastError();
+    return launch_send_kernel(kern, grid, L::kThreads, L::kSmemBytes, ta, tb, p, s);
 }
 
 cudaError_t launch_gemm_send_fp8(const CUtensorMap &ta, const CUtensorMap &tb,

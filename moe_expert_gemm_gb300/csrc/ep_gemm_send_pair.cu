@@ -100,6 +100,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
         tma_prefetch_map(&tmap_a);
         tma_prefetch_map(&tmap_b);
     }
+    griddep_wait();  // from here on global memory may be what the previous kernel wrote
     sink_prologue(p, sh, L::kTileRows);
     tc_fence_before();
     __syncthreads();
@@ -372,8 +373,8 @@ cudaError_t launch_gemm_send_bf16_pair(const CUtensorMap &ta, const CUtensorMap 
         active = max_pairs;
     }
     const int pairs = active < max_pairs ? active : max_pairs;
-    gemm_send_bf16_pair_kernel<<<2 * pairs, L::kThreads, L::kSmemBytes, s>>>(ta, tb, p);
-    return cudaGetLastError();
+    return launch_send_kernel(gemm_send_bf16_pair_kernel, 2 * pairs, L::kThreads, L::kSmemBytes,
+                              ta, tb, p, s);
 }
 
 }  // namespace ep

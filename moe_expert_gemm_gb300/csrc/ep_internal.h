@@ -41,7 +41,28 @@ struct SendParams {
     const float *w_scales;
     uint64_t *trace;    // optional per-tile timestamps
     int trace_records;  // records per thread block
+    int overlap_previous;  // launched as a programmatic dependent of the previous kernel
 };
+
+// Launch of a fused send kernel, as a programmatic dependent of the previous kernel
+// on the stream when p.overlap_previous is set.
+template <typename Kern>
+inline cudaError_t launch_send_kernel(Kern kern, int grid, int threads, int smem,
+                                      const CUtensorMap &ta, const CUtensorMap &tb,
+                                      const SendParams &p, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.overlap_previous ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+}
 
 // The unfused send step (local C rows to the receive buffers, then signalling).
 struct ScatterParams {

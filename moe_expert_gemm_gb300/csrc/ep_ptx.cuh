@@ -474,6 +474,13 @@ __device__ __forceinline__ void griddep_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Launched as a programmatic dependent: wait until the grids this one depends on have
+// completed and their memory operations are visible (a no-op otherwise).
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // SiLU(x) = x / (1 + e^-x) in fp32 (expf of the CUDA math library).
 __device__ __forceinline__ float silu_f32(float x)
 {

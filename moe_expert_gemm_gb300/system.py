@@ -138,9 +138,14 @@ class EpSystem:
         a.timeout_ns = self.timeout_ns
         return a
 
-    def send(self, rank: int, epoch: int, stream=None, p3_control: int = 0, C=None):
-        grouped_gemm_combine_send(self.cfg(rank), self.send_args(rank, epoch, p3_control, C),
-                                  stream)
+    def send(self, rank: int, epoch: int, stream=None, p3_control: int = 0, C=None,
+             overlap: bool = False):
+        """``overlap``: may start while the kernel before it on the stream is still
+        finishing (programmatic dependent launch; it reads nothing before that kernel
+        has completed)."""
+        a = self.send_args(rank, epoch, p3_control, C)
+        a.overlap_previous = 1 if overlap else 0
+        grouped_gemm_combine_send(self.cfg(rank), a, stream)
 
     def local_C(self, rank: int):
         """A [max_rows][N] bf16 buffer for the unfused path's local GEMM output."""
@@ -206,12 +211,14 @@ class EpSystem:
                          2 * self.K, 4 * self.K, EP_BF16, self.send_warps, self.signal_mode)
 
     def layer_forward(self, rank: int, epoch: int, stream=None, p3_control: int = 0,
-                      events=None, fused_act: bool = False):
+                      events=None, fused_act: bool = False, overlap: bool = False):
         """Dispatch, up/gate GEMM, activation, then the fused down-projection + send
         of producer ``rank`` (every ``layer[r]["X"]`` must hold rank r's tokens).
         ``fused_act``: the activation runs in the up/gate GEMM's epilogue (interleaved
         W1, no G) instead of as its own pass. ``events``: four CUDA events recorded
-        after each of the first four steps."""
+        after each of the first four steps. ``overlap``: the two GEMM calls launch as
+        programmatic dependents of the kernel before them (their set-up overlaps its
+        end); ignored when ``events`` are recorded between the steps."""
         L, p = self.layer[rank], self.plans[rank]
         mark = (lambda i: events[i].record(stream)) if events is not None else (lambda i: None)
         d = ep_dispatch_args()
@@ -231,6 +238,8 @@ class EpSystem:
         up.max_rows = int(L["A_in"].shape[0])
         if fused_act:
             up.local_activation = EP_ACT_SWIGLU
+        overlap = overlap and events is None
+        up.overlap_previous = 1 if overlap else 0
         grouped_gemm_combine_send(self.cfg_up(rank), up, stream)
         mark(1)
         if not fused_act:
@@ -238,7 +247,7 @@ class EpSystem:
                                ptr(p["expert_offsets"]), int(L["G"].shape[0]), self.K)
             ep_swiglu(self.cfg(rank), a, stream)
         mark(2)
-        self.send(rank, epoch, stream, p3_control=p3_control)
+        self.send(rank, epoch, stream, p3_control=p3_control, overlap=overlap)
         mark(3)
 
     def send_traced(self, rank: int, epoch: int, records: int = 64, stream=None):

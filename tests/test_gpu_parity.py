@@ -26,6 +26,13 @@ def _check_full(w, routing=None, values=None, epoch=3, send_warps=-1, unfused=Fa
     s = build_system(w, routing, values, send_warps=send_warps, signal_mode=int(per_expert))
     run_all(s, epoch, unfused)
     torch.cuda.synchronize()
+    ref = _assert_matches_oracle(s, w, routing, values, epoch, per_expert)
+    return s, ref, routing, values
+
+
+def _assert_matches_oracle(s, w, routing, values, epoch, per_expert=False):
+    """Plans, count and flag words bit for bit; received rows and combined outputs of
+    every rank within the tolerance; counters re-armed; no status bit."""
     st = s.status_words()
     assert (st == 0).all(), st
     ref = full_pipeline(w, routing, values, epoch=epoch, per_expert=per_expert)
@@ -43,7 +50,7 @@ def _check_full(w, routing=None, values=None, epoch=3, send_warps=-1, unfused=Fa
     for r in range(w.n_ranks):  # counters re-armed for the next call
         assert int(s.atomic_counter[r].abs().sum()) == 0
         assert int(s.rank_counter[r].abs().sum()) == 0
-    return s, ref, routing, values
+    return ref
 
 
 def test_tiny_full_parity():
@@ -415,3 +422,30 @@ def test_combine_overlapping_the_fused_send(name, w, signal_mode):
         out = s.out[d].view(torch.int16).cpu().numpy().view(np.uint16)
         assert combine_rel_err(out, ref["out_exact"][d], ref["rows_exact"][d],
                                routing.gates[d]) <= TOL[w.dtype], d
+
+
+SEND_OVERLAP_CASES = [
+    ("tiny", WORKLOADS["tiny"]),
+    ("qwen_shape_small", _EDGE["qwen_shape_small"]),
+    ("pair_shape", Workload("so_pair", 4, 3, 2, 400, 320, 512, "bf16", "zipf", "softmax_sel", 78)),
+    ("fp8_small", _EDGE["fp8_small"]),
+]
+
+
+@pytest.mark.parametrize("name,w", SEND_OVERLAP_CASES, ids=[c[0] for c in SEND_OVERLAP_CASES])
+def test_send_overlapping_the_plan_that_feeds_it(name, w):
+    """Each rank's plan is recomputed into fresh buffers by the kernel right before an
+    overlapped send (a programmatic dependent of it), and each combine overlaps the
+    send before it: the send must read the plan only after the plan kernel's memory
+    is visible, and the results must be the oracle's."""
+    routing, values = make_inputs(w)
+    s = build_system(w, routing, values)
+    torch.cuda.synchronize()
+    epoch = 4
+    for r in range(w.n_ranks):
+        s.plan(r)
+        s.send(r, epoch, overlap=True)
+    for d in range(w.n_ranks):
+        s.combine(d, epoch, overlap=True)
+    torch.cuda.synchronize()
+    _assert_matches_oracle(s, w, routing, values, epoch)
