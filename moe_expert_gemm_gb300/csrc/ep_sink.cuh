@@ -292,9 +292,9 @@ __device__ __forceinline__ void close_queue(SinkShared *sh)
 
 // Completion warp, one thread: counts finished tiles per expert (one gpu-scope
 // release fence per batch of tiles) and runs the signalling of every expert this
-// block completes (count stores, one system-scope acquire-release fence for the
-// batch, election). Block 0 also signals the experts without rows, which have no
-// tile to complete.
+// block completes (rank flag: count stores, one gpu-scope acquire-release fence for
+// the batch, election; per expert: one system-scope fence, tagged count words).
+// Block 0 also signals the experts without rows, which have no tile to complete.
 static __device__ void completion_loop(const SendParams &p, SinkShared *sh)
 {
     volatile int *head_p = &sh->q_head;
