@@ -102,6 +102,13 @@ EDGE = [
                                     "softmax_sel", 73), "random"),
     ("many_local_experts_pairs", Workload("many_el_pair", 1, 40, 8, 1300, 128, 256, "bf16",
                                           "uniform", "softmax_sel", 74), "random"),
+    # E_l * n_ranks above the kernels' shared-memory count cache (512 words): the
+    # count words are read from the plan in global memory
+    ("count_words_past_the_cache", Workload("many_counts", 8, 72, 2, 24, 128, 128, "bf16",
+                                            "uniform", "softmax_sel", 79), "random"),
+    # a rank whose experts receive no row at all still signals (counts 0 and its flag)
+    ("rank_without_rows", Workload("idle_rank", 4, 2, 2, 40, 128, 256, "bf16", "uniform",
+                                   "softmax_sel", 80), "idle_rank"),
     # a top_k with no specialised combine (3)
     ("topk3", Workload("topk3", 4, 2, 3, 40, 128, 256, "bf16", "uniform", "softmax_sel", 55),
      "random"),
@@ -126,6 +133,13 @@ def test_edge_parity(name, w, kind):
     routing = make_routing(w)
     if kind == "hot":
         ids = np.tile(np.array([2, 3], np.int32), (w.n_ranks, w.tokens, 1))
+        routing = _fixed_routing(w, ids)
+    elif kind == "idle_rank":
+        # experts 2 and 3 (rank 1's) receive nothing
+        rng = np.random.default_rng(11)
+        choices = np.array([0, 1, 4, 5, 6, 7], np.int32)
+        ids = np.stack([np.stack([rng.choice(choices, w.top_k, replace=False)
+                                  for _ in range(w.tokens)]) for _ in range(w.n_ranks)])
         routing = _fixed_routing(w, ids)
     elif kind == "empty":
         # only experts 0, 5, 6 and 13 receive rows; every rank keeps at least one empty expert
@@ -346,6 +360,7 @@ PER_EXPERT_CASES = [
      False),
     ("fp8_small", _EDGE["fp8_small"], False),
     ("many_local_experts", _EDGE["many_local_experts"], False),
+    ("count_words_past_the_cache", _EDGE["count_words_past_the_cache"], False),
     ("tiny_unfused", WORKLOADS["tiny"], True),
 ]
 
