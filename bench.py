@@ -75,9 +75,11 @@ def parse_args():
     ap.add_argument("--layer-act", choices=["fused", "separate"], default="fused",
                     help="--path layer: the activation in the up/gate GEMM's epilogue (fused) "
                          "or as its own pass over the GEMM's rows (separate)")
-    ap.add_argument("--no-overlap", action="store_true",
-                    help="launch the combine after the fused send has ended instead of as a "
-                         "programmatic dependent that starts while the send finishes")
+    ap.add_argument("--overlap", action="store_true",
+                    help="launch the combine (and, for --path layer, the two GEMMs) as a "
+                         "programmatic dependent that starts while the kernel before it "
+                         "finishes; the per-kernel times then come from a serialised copy of "
+                         "every timed step, run right after it")
     ap.add_argument("--signal-mode", choices=["rank_flag", "per_expert"], default="rank_flag",
                     help="completion signalling: ep_ord_r rank flags (default) or per-expert "
                          "count words with a per-token wait in the combine")
@@ -410,7 +412,7 @@ def main():
     # the combine may start while the fused send finishes (its rows are ordered by the
     # flags it acquires, not by the kernel boundary); the per-kernel breakdown is taken
     # from separately timed steps with the two kernels serialised
-    overlap = not args.no_overlap and not unfused
+    overlap = args.overlap and not unfused
 
     def one_step(evs=None, serial=False):
         e = epoch[0]
@@ -448,20 +450,22 @@ def main():
     clocks.start()
     time.sleep(0.5)  # let the sampler start before the timed region
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    # with overlap, every timed step is followed by the same step with its kernels
+    # serialised, which gives the per-kernel times under the same clocks and power
+    serial_events = ([[torch.cuda.Event(enable_timing=True) for _ in range(8)]
+                      for _ in range(args.steps)] if overlap else None)
     torch.cuda.synchronize()
     for i in range(args.steps):
         one_step(events[i])
+        if overlap:
+            one_step(serial_events[i], serial=True)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     step_overlapped = (statistics.mean(e[0].elapsed_time(e[2]) for e in events)
                        if overlap else None)
-    if overlap:  # per-kernel times: the same steps with the kernels serialised
-        events = [[torch.cuda.Event(enable_timing=True) for _ in range(8)]
-                  for _ in range(args.steps)]
-        for i in range(args.steps):
-            one_step(events[i], serial=True)
-        torch.cuda.synchronize()
+    if overlap:
+        events = serial_events
     clk = clocks.stop()
     send_ms = [e[0].elapsed_time(e[1]) for e in events]
     comb_ms = [e[1].elapsed_time(e[2]) for e in events]
@@ -634,9 +638,10 @@ def main():
                         "ep_combine_reduce": statistics.mean(comb_ms)}),
         "combine_gbs": comb_bytes / comb_s / 1e9,
         "roofline": roof,
-        # dispatch, up/gate GEMM (+ ep_swiglu when separate), send, combine
+        # dispatch, up/gate GEMM (+ ep_swiglu when separate), send, combine; with overlap
+        # the serialised copy of every step runs inside the timed loop as well
         "gpu_launches": ((4 if args.layer_act == "fused" else 5) if layer
-                         else 3 if unfused else 2) * args.steps,
+                         else 3 if unfused else 2) * args.steps * (2 if overlap else 1),
         "clocks": clk,
     }
     if e2e is not None:
