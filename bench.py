@@ -437,7 +437,9 @@ def main():
         if evs is not None and (serial or not overlap):
             evs[1].record(stream)
         if not args.solo:
-            s.combine(q, e, stream, overlap=overlap and not serial)
+            # the kernel before the combine is the send, which writes none of its inputs
+            s.combine(q, e, stream, overlap=ep.EP_OVERLAP_INPUTS_READY
+                      if overlap and not serial else ep.EP_OVERLAP_NONE)
         if evs is not None:
             evs[2].record(stream)
 
@@ -534,9 +536,9 @@ def main():
             if fp8:
                 a.a_scales = ep.ptr(sa_bufs[b])
             ep.grouped_gemm_combine_send(cfg_q, a, stream)
-            ep.ep_combine_reduce(cfg_q, s.combine_args(q, e, gates=g_bufs[b], out=o_bufs[b],
-                                                       overlap=overlap),
-                                 stream)
+            ep.ep_combine_reduce(cfg_q, s.combine_args(
+                q, e, gates=g_bufs[b], out=o_bufs[b],
+                overlap=ep.EP_OVERLAP_INPUTS_READY if overlap else ep.EP_OVERLAP_NONE), stream)
             inputs_free[b] = stream.record_event()
             d2h_stream.wait_event(inputs_free[b])
             with torch.cuda.stream(d2h_stream):

@@ -404,18 +404,26 @@ int ep_swiglu(const ep_config *cfg, const ep_swiglu_args *args, ep_stream_t stre
  *               and the affected outputs are left unwritten
  *   topk_ids    EP_SIGNAL_PER_EXPERT only: this rank's routing, [num_tokens][top_k]
  *               global expert ids (the table ep_plan reads, rank my_rank's part)
- *   overlap_previous  nonzero: launch as a programmatic dependent of the previous
- *               kernel on `stream`, so that when that kernel is this library's fused
- *               send (which signals its dependents as its thread blocks finish) the
- *               combine starts before the send has fully ended. Safe because the
- *               combine reads no row before acquiring the signal that releases it;
- *               after any other kernel it simply waits for its completion.
+ *   overlap_previous  EP_OVERLAP_NONE (0): launch after the previous work on `stream`
+ *               has ended. EP_OVERLAP_ANY: launch as a programmatic dependent of the
+ *               previous kernel on `stream`; the combine reads no row before acquiring
+ *               the signal that releases it, and reads the gates, the routing and `out`
+ *               only after the previous kernel has completed and its memory is visible
+ *               (with the rank flags it acquires the flags first, so that this wait
+ *               overlaps the end of a send). EP_OVERLAP_INPUTS_READY: the same launch
+ *               for a caller that guarantees the previous kernel writes none of the
+ *               gates, the routing and `out` (e.g. it is this library's fused send):
+ *               no wait, so the combine's reads start while that kernel finishes.
  * EP_SIGNAL_RANK_FLAG: each thread block acquires every source rank's flag once
  * (system scope) before reading the rows, as the fused consumer of
  * "ep_signal_completion" does. EP_SIGNAL_PER_EXPERT: before reducing a token, the
  * warp acquires the count words of that token's top_k experts, so tokens whose
  * experts have all arrived are reduced even while other experts are still sending.
  */
+#define EP_OVERLAP_NONE 0
+#define EP_OVERLAP_ANY 1
+#define EP_OVERLAP_INPUTS_READY 2
+
 typedef struct {
     const uint8_t *recv_buf;
     const uint64_t *recv_count;

@@ -29,6 +29,9 @@ EP_ACT_NONE = 0
 EP_ACT_SWIGLU = 1
 EP_SIGNAL_RANK_FLAG = 0
 EP_SIGNAL_PER_EXPERT = 1
+EP_OVERLAP_NONE = 0
+EP_OVERLAP_ANY = 1
+EP_OVERLAP_INPUTS_READY = 2
 EP_STATUS_ROUTING = 0x8
 EP_STATUS_INTERNAL = 0x10
 

@@ -430,6 +430,8 @@ int ep_combine_reduce(const ep_config *cfg, const ep_combine_args *a, ep_stream_
     if (cfg->N % 8 != 0 || !aligned16(a->recv_buf) || (a->out && !aligned16(a->out)) ||
         (reinterpret_cast<uintptr_t>(a->recv_count) & 7u))
         return EP_ERR_INVALID_ARG;
+    if (a->overlap_previous < EP_OVERLAP_NONE || a->overlap_previous > EP_OVERLAP_INPUTS_READY)
+        return EP_ERR_INVALID_ARG;
     const int num_sms = sm_count();
     if (num_sms <= 0)
         return EP_ERR_CUDA;
@@ -449,7 +451,7 @@ int ep_combine_reduce(const ep_config *cfg, const ep_combine_args *a, ep_stream_
     p.status = a->status;
     p.topk_ids = a->topk_ids;
     p.signal_mode = cfg->signal_mode;
-    p.overlap_previous = a->overlap_previous != 0 ? 1 : 0;
+    p.overlap_previous = a->overlap_previous;
     return cuda_status(ep::launch_combine(p, num_sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 

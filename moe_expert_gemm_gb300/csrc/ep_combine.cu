@@ -89,6 +89,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 {
     if (!acquire_source_flags(p))
         return;
+    if (p.overlap_previous == EP_OVERLAP_ANY)
+        griddep_wait();  // gates (and out) may belong to the kernel before this one
     const int lane = threadIdx.x & 31;
     const int warps = kCombineThreads / 32;
     const int64_t vec_per_row = p.N / 8;  // 16-byte vectors of one output row
@@ -191,6 +193,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel_per_expert(con
     __shared__ int s_gave_up;
     if (threadIdx.x == 0)
         s_gave_up = 0;
+    if (p.overlap_previous == EP_OVERLAP_ANY)
+        griddep_wait();  // the routing and gates may belong to the kernel before this one
     __syncthreads();
     volatile int *gave_up = &s_gave_up;
     const int k = K == 0 ? p.top_k : K;
@@ -271,6 +275,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel_any(const Comb
 {
     if (!acquire_source_flags(p))
         return;
+    if (p.overlap_previous == EP_OVERLAP_ANY)
+        griddep_wait();  // gates (and out) may belong to the kernel before this one
     const int lane = threadIdx.x & 31;
     const int warps = kCombineThreads / 32;
     const int k = p.top_k;

@@ -121,7 +121,7 @@ struct CombineParams {
     uint32_t *status;
     const int32_t *topk_ids;  // EP_SIGNAL_PER_EXPERT: [T][top_k] global expert ids
     int signal_mode;
-    int overlap_previous;  // launch as a programmatic dependent of the previous kernel
+    int overlap_previous;  // EP_OVERLAP_*: programmatic dependent of the previous kernel
 };
 
 // Kernel launchers; each returns the launch's cudaError_t.

@@ -263,19 +263,21 @@ class EpSystem:
         return decode_trace(buf.cpu().numpy().view(np.uint64), n_sm, records)
 
     def combine_args(self, rank: int, epoch: int, gates=None, out=None,
-                     overlap: bool = False) -> ep_combine_args:
+                     overlap: int = 0) -> ep_combine_args:
         g = self.gates[rank] if gates is None else gates
         o = self.out[rank] if out is None else out
         return ep_combine_args(ptr(self.recv[rank]), ptr(self.counts[rank]), ptr(g), ptr(o),
                                epoch, self.timeout_ns,
                                self.status.data_ptr() + 4 * STATUS_COMBINE,
                                ptr(self.topk[rank]) if self.topk is not None else 0,
-                               1 if overlap else 0)
+                               int(overlap))
 
     def combine(self, rank: int, epoch: int, stream=None, gates=None, out=None,
-                overlap: bool = False):
-        """``overlap``: may start while the fused send before it on the stream is still
-        finishing (programmatic dependent launch)."""
+                overlap: int = 0):
+        """``overlap``: EP_OVERLAP_* (True is EP_OVERLAP_ANY): may start while the kernel
+        before it on the stream is still finishing (programmatic dependent launch);
+        EP_OVERLAP_INPUTS_READY when that kernel writes none of the gates, routing or
+        output (e.g. it is the fused send)."""
         ep_combine_reduce(self.cfg(rank), self.combine_args(rank, epoch, gates, out, overlap),
                           stream)
 

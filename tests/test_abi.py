@@ -163,6 +163,13 @@ def test_per_expert_combine_needs_the_routing(lib):
         ep.EP_ERR_INVALID_ARG
 
 
+def test_combine_overlap_mode_is_checked(lib):
+    cfg = _cfg()
+    a = ep.ep_combine_args(0x1000000, 0x2000000, 0x3000000, 0x4000000, 1, 0, 0x5000000, 0, 3)
+    assert lib.ep_combine_reduce(ctypes.byref(cfg), ctypes.byref(a), None) == \
+        ep.EP_ERR_INVALID_ARG
+
+
 def test_strerror(lib):
     assert ep.ep_strerror(ep.EP_ERR_UNSUPPORTED) == "unsupported configuration"
     assert "timed out" in ep.ep_strerror(ep.EP_STATUS_TIMEOUT)

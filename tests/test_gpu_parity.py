@@ -430,7 +430,7 @@ def test_combine_overlapping_the_fused_send(name, w, signal_mode):
             if r != d:
                 s.send(r, epoch=10 + d)
         s.send(d, epoch=10 + d)  # d's own send, then its combine right behind it
-        s.combine(d, epoch=10 + d, overlap=True)
+        s.combine(d, epoch=10 + d, overlap=ep.EP_OVERLAP_INPUTS_READY)
         torch.cuda.synchronize()
         assert (s.status_words() == 0).all(), (d, s.status_words())
         ref = full_pipeline(w, routing, values, epoch=10 + d, per_expert=bool(signal_mode))
@@ -461,6 +461,30 @@ def test_send_overlapping_the_plan_that_feeds_it(name, w):
         s.plan(r)
         s.send(r, epoch, overlap=True)
     for d in range(w.n_ranks):
-        s.combine(d, epoch, overlap=True)
+        s.combine(d, epoch, overlap=ep.EP_OVERLAP_INPUTS_READY)
     torch.cuda.synchronize()
     _assert_matches_oracle(s, w, routing, values, epoch)
+
+
+def test_combine_overlapping_the_kernel_that_writes_its_gates():
+    """The combine launched as a programmatic dependent of a kernel that writes its
+    gates (an elementwise kernel right before it) reads the new gates: it waits for
+    that kernel's completion before reading them."""
+    w = WORKLOADS["tiny"]
+    routing, values = make_inputs(w)
+    s = build_system(w, routing, values)
+    run_all(s, 1)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(21)
+    g2 = rng.random(routing.gates.shape).astype(np.float32) + 0.1
+    g2 /= g2.sum(-1, keepdims=True)
+    g2_dev = torch.from_numpy(g2).cuda()
+    for d in range(w.n_ranks):
+        torch.mul(g2_dev[d], 1.0, out=s.gates[d])  # a kernel, right before the combine
+        s.combine(d, epoch=1, overlap=ep.EP_OVERLAP_ANY)
+    torch.cuda.synchronize()
+    assert (s.status_words() == 0).all()
+    ref = full_pipeline(w, Routing(routing.topk_ids, g2), values, epoch=1)
+    for d in range(w.n_ranks):
+        out = s.out[d].view(torch.int16).cpu().numpy().view(np.uint16)
+        assert combine_rel_err(out, ref["out_exact"][d], ref["rows_exact"][d], g2[d]) <= TOL["bf16"]
