@@ -70,3 +70,25 @@ def test_single_process_helpers():
     assert bench.replica_rank(9, 8) == 1
     assert bench.replica_rank(3, 8, first=6) == 1  # replicas start from the timed rank
     assert bench.job_tokens_per_s(1, 1000, 2.0) == 500_000.0
+
+
+def test_reference_arm_line_on_rank_0():
+    """The reference arm's JSON line (the oracle on the host, tiny workload): the keys
+    the driver reads, its cpu_baseline describing the run, and an e2e equal to it."""
+    import argparse
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    out = io.StringIO()
+    with redirect_stdout(out):
+        bench.run_reference(argparse.Namespace(workload="tiny", steps=2, warmup=1, rank="1"), 0, 1)
+    line = json.loads(out.getvalue().strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "tokens/s"
+    assert line["steps"] == 2 and line["warmup"] == 1 and line["n_gpus"] == 1
+    assert line["higher_is_better"] is True and line["value"] > 0
+    assert line["config"]["workload"] == "tiny" and line["config"]["my_rank"] == 1
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    assert "rank 1" in cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
