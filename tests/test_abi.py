@@ -148,6 +148,22 @@ def test_fp8_shape_rules(lib):
             ep.EP_ERR_UNSUPPORTED
 
 
+def test_bf16_shape_rules(lib):
+    """bf16 needs whole 128-byte K atoms and 64-column output chunks; the activation
+    epilogue pairs the halves of 256-column tiles."""
+    a = ep.ep_send_args()
+    for kw in (dict(K=96), dict(N=96, msg_bytes=192)):
+        cfg = _cfg(**kw)
+        assert lib.grouped_gemm_combine_send(ctypes.byref(cfg), ctypes.byref(a), None) == \
+            ep.EP_ERR_UNSUPPORTED
+    act = ep.ep_send_args()
+    act.p3_control = -1
+    act.local_activation = ep.EP_ACT_SWIGLU
+    cfg = _cfg(N=192, msg_bytes=384)
+    assert lib.grouped_gemm_combine_send(ctypes.byref(cfg), ctypes.byref(act), None) == \
+        ep.EP_ERR_UNSUPPORTED
+
+
 def test_fp8_has_no_dedicated_send_warps(lib):
     """Dedicated send warps exist in the bf16 kernel only."""
     cfg = _cfg(dtype=ep.EP_FP8_1D2D, send_warps=4)
