@@ -17,3 +17,17 @@ def oracle_lib():
     import oracle
     oracle.build()
     return oracle
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """EP_PARITY_LOG=<file>: write every combined-output comparison (both metrics)."""
+    path = os.environ.get("EP_PARITY_LOG")
+    if not path:
+        return
+    try:
+        from parity_util import PARITY_LOG
+    except ImportError:
+        return
+    import json
+    with open(path, "w") as f:
+        json.dump(PARITY_LOG, f, indent=1)

@@ -12,6 +12,16 @@ which bounds its error by 2^-8 + 2^-8 = 2^-7 of that scale; comparing instead
 with the oracle's own twice-rounded value would double that bound, since two
 correctly rounded chains may land two ulps apart. Indices, counts and flags are
 compared bit for bit.
+
+The survey's own metric for combined outputs (its reading R14),
+max_i |g_i - r_i| / max(|r_i|, rms(r)) against the exact value, is computed on
+every combined output as well and asserted at the same tolerance wherever a
+correctly rounded result can meet it: the oracle's own twice-rounded output is
+the witness. Where even that output exceeds the tolerance (a bf16 chain that
+rounds the received rows and then the sum can sit up to 2^-7 of
+sum_j g|y_j| away from the exact value, which exceeds 1e-2 of rms(r) at
+cancellation points), only the bound above applies; every value is recorded
+(``PARITY_LOG``) and written out when EP_PARITY_LOG names a file.
 """
 
 from __future__ import annotations
@@ -52,6 +62,42 @@ def combine_rel_err(got_bits, ref_exact, rows_exact, gates) -> float:
     scale = np.einsum("tj,tjn->tn", np.asarray(gates, np.float64), y)
     den = np.maximum(np.maximum(np.abs(r), scale), 1e-30)
     return float(np.max(np.abs(g - r) / den))
+
+
+def r14_rel_err(got_bits, ref) -> float:
+    """max_i |g_i - r_i| / max(|r_i|, rms(r)) of bf16 outputs against float64 (or
+    bf16-bit) reference values r."""
+    g = bf16_to_f32(got_bits).astype(np.float64)
+    r = np.asarray(ref)
+    r = bf16_to_f32(r).astype(np.float64) if r.dtype == np.uint16 else r.astype(np.float64)
+    if g.size == 0:
+        return 0.0
+    if np.isnan(g).any():
+        return float("inf")
+    rms = np.sqrt(np.mean(r * r))
+    den = np.maximum(np.abs(r), max(rms, 1e-30))
+    return float(np.max(np.abs(g - r) / den))
+
+
+PARITY_LOG: list = []
+
+
+def assert_combine_close(got_bits, oracle_bits, out_exact, rows_exact, gates, tol,
+                         where="") -> dict:
+    """Combined outputs against the oracle: the scaled bound (always), and the
+    survey's R14 metric against the exact value wherever the oracle's own
+    correctly rounded output meets it. Returns (and records) the three values."""
+    scaled = combine_rel_err(got_bits, out_exact, rows_exact, gates)
+    r14 = r14_rel_err(got_bits, out_exact)
+    witness = r14_rel_err(oracle_bits, out_exact)
+    rec = dict(where=str(where), tol=tol, scaled=scaled, r14_exact=r14,
+               r14_oracle_rounded=witness, r14_vs_oracle=r14_rel_err(got_bits, oracle_bits),
+               r14_asserted=witness <= tol)
+    PARITY_LOG.append(rec)
+    assert scaled <= tol, rec
+    if witness <= tol:
+        assert r14 <= tol, rec
+    return rec
 
 
 def make_inputs(w, routing=None):

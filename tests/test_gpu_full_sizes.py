@@ -10,8 +10,8 @@ import torch
 
 import oracle
 from oracle.pipeline import SENTINEL_WORD, sampled_pipeline
-from parity_util import (TOL, assert_plan_equal, build_system, combine_rel_err, make_inputs,
-                         max_rel_err)
+from parity_util import (TOL, assert_combine_close, assert_plan_equal, build_system,
+                         make_inputs, max_rel_err)
 from synth import WORKLOADS, Workload
 
 pytestmark = pytest.mark.gpu
@@ -70,8 +70,8 @@ def test_full_size_sampled_parity(name, path, signal_mode):
     tol = TOL[w.dtype]
     assert max_rel_err(recv0[toks], ref["rows"]) <= tol
     out0 = s.out[0].view(torch.int16).cpu().numpy().view(np.uint16)
-    assert combine_rel_err(out0[toks], ref["out_exact"], ref["rows_exact"],
-                           routing.gates[0][toks]) <= tol
+    assert_combine_close(out0[toks], ref["out"], ref["out_exact"], ref["rows_exact"],
+                         routing.gates[0][toks], tol, (w.name, "sampled", 0))
 
     # rows rank 0 produced for the other ranks
     p0 = plans[0]

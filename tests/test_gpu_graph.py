@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from oracle.pipeline import full_pipeline
-from parity_util import TOL, build_system, combine_rel_err, make_inputs, max_rel_err
+from parity_util import TOL, assert_combine_close, build_system, make_inputs, max_rel_err
 from synth import WORKLOADS, Workload
 
 pytestmark = pytest.mark.gpu
@@ -79,5 +79,5 @@ def test_send_and_combine_replayed_from_a_cuda_graph(name, w):
             assert max_rel_err(s.recv[d].cpu().numpy().view(np.uint16),
                                ref["recv"][d].view(np.uint16)) <= tol, (rep, d)
             out = s.out[d].view(torch.int16).cpu().numpy().view(np.uint16)
-            assert combine_rel_err(out, ref["out_exact"][d], ref["rows_exact"][d],
-                                   routing.gates[d]) <= tol, (rep, d)
+            assert_combine_close(out, ref["out"][d], ref["out_exact"][d], ref["rows_exact"][d],
+                                 routing.gates[d], tol, (w.name, "graph", rep, d))

@@ -19,7 +19,7 @@ import torch
 from moe_expert_gemm_gb300.system import EpSystem
 import oracle
 from oracle.pipeline import full_pipeline, layer_pipeline
-from parity_util import TOL, combine_rel_err, max_rel_err
+from parity_util import TOL, assert_combine_close, max_rel_err
 from synth import Workload, WORKLOADS, make_layer_values, make_routing
 
 pytestmark = pytest.mark.gpu
@@ -78,5 +78,5 @@ def test_layer_parity(name, w, fused_act):
         got = s.recv[d].cpu().numpy().view(np.uint16)
         assert max_rel_err(got, down["recv"][d].view(np.uint16)) <= TOL["bf16"], d
         out = s.out[d].view(torch.int16).cpu().numpy().view(np.uint16)
-        assert combine_rel_err(out, down["out_exact"][d], down["rows_exact"][d],
-                               routing.gates[d]) <= TOL["bf16"], d
+        assert_combine_close(out, down["out"][d], down["out_exact"][d], down["rows_exact"][d],
+                             routing.gates[d], TOL["bf16"], (w.name, "layer", d))

@@ -13,8 +13,8 @@ import torch
 import moe_expert_gemm_gb300 as ep
 import oracle
 from oracle.pipeline import full_pipeline
-from parity_util import (TOL, assert_plan_equal, build_system, combine_rel_err, make_inputs,
-                         max_rel_err, run_all)
+from parity_util import (TOL, assert_combine_close, assert_plan_equal, build_system,
+                         make_inputs, max_rel_err, run_all)
 from synth import Routing, Workload, WORKLOADS, make_routing
 
 pytestmark = pytest.mark.gpu
@@ -45,8 +45,8 @@ def _assert_matches_oracle(s, w, routing, values, epoch, per_expert=False):
         want = ref["recv"][d].view(np.uint16)
         assert max_rel_err(got, want) <= tol, d
         out = s.out[d].view(torch.int16).cpu().numpy().view(np.uint16)
-        assert combine_rel_err(out, ref["out_exact"][d], ref["rows_exact"][d],
-                               routing.gates[d]) <= tol, d
+        assert_combine_close(out, ref["out"][d], ref["out_exact"][d], ref["rows_exact"][d],
+                             routing.gates[d], tol, (w.name, d))
     for r in range(w.n_ranks):  # counters re-armed for the next call
         assert int(s.atomic_counter[r].abs().sum()) == 0
         assert int(s.rank_counter[r].abs().sum()) == 0
@@ -67,8 +67,8 @@ def test_tiny_two_epochs_in_a_row():
     for d in range(w.n_ranks):
         np.testing.assert_array_equal(s.counts[d].cpu().numpy().view(np.uint64), ref2["counts"][d])
         out = s.out[d].view(torch.int16).cpu().numpy().view(np.uint16)
-        assert combine_rel_err(out, ref2["out_exact"][d], ref2["rows_exact"][d],
-                               routing.gates[d]) <= TOL[w.dtype]
+        assert_combine_close(out, ref2["out"][d], ref2["out_exact"][d], ref2["rows_exact"][d],
+                             routing.gates[d], TOL[w.dtype], (w.name, "epoch 2", d))
 
 
 def _fixed_routing(w, ids, seed=5):
@@ -403,8 +403,9 @@ def test_per_expert_tokens_of_finished_ranks_are_combined_while_one_rank_is_miss
         waits = missing[d].any(axis=1)
         assert waits.any() and (~waits).any()
         assert (out[waits] == 0).all()
-        assert combine_rel_err(out[~waits], ref["out_exact"][d][~waits],
-                               ref["rows_exact"][d][~waits], routing.gates[d][~waits]) <= TOL["bf16"]
+        assert_combine_close(out[~waits], ref["out"][d][~waits], ref["out_exact"][d][~waits],
+                             ref["rows_exact"][d][~waits], routing.gates[d][~waits], TOL["bf16"],
+                             (w.name, "missing rank", d))
 
 
 OVERLAP_CASES = [
@@ -435,8 +436,8 @@ def test_combine_overlapping_the_fused_send(name, w, signal_mode):
         assert (s.status_words() == 0).all(), (d, s.status_words())
         ref = full_pipeline(w, routing, values, epoch=10 + d, per_expert=bool(signal_mode))
         out = s.out[d].view(torch.int16).cpu().numpy().view(np.uint16)
-        assert combine_rel_err(out, ref["out_exact"][d], ref["rows_exact"][d],
-                               routing.gates[d]) <= TOL[w.dtype], d
+        assert_combine_close(out, ref["out"][d], ref["out_exact"][d], ref["rows_exact"][d],
+                             routing.gates[d], TOL[w.dtype], (w.name, "overlap", d))
 
 
 SEND_OVERLAP_CASES = [
@@ -487,4 +488,5 @@ def test_combine_overlapping_the_kernel_that_writes_its_gates():
     ref = full_pipeline(w, Routing(routing.topk_ids, g2), values, epoch=1)
     for d in range(w.n_ranks):
         out = s.out[d].view(torch.int16).cpu().numpy().view(np.uint16)
-        assert combine_rel_err(out, ref["out_exact"][d], ref["rows_exact"][d], g2[d]) <= TOL["bf16"]
+        assert_combine_close(out, ref["out"][d], ref["out_exact"][d], ref["rows_exact"][d], g2[d],
+                             TOL["bf16"], (w.name, "gate writer", d))

@@ -508,6 +508,42 @@ def test_swiglu_matches_an_independent_form_and_special_values():
     assert abs(A2[1] - 90.0) <= 0.5 and abs(A2[2]) < 1e-9
 
 
+def _bf16_rne_f64(x: np.ndarray) -> np.ndarray:
+    """Round float64 values (normal bf16 range) to the nearest bf16 value, ties to
+    even, as float64: 8 significant bits, written out from the definition."""
+    m, e = np.frexp(np.asarray(x, np.float64))  # x = m * 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+
+
+def test_swiglu_exact_matches_an_independent_form_and_special_values():
+    """The activation of the unrounded products (the epilogue form): SiLU(g) * u with
+    SiLU(x) = (x / 2) * (1 + tanh(x / 2)), evaluated independently in float64 and
+    rounded once to bf16 by a separate restatement of round-to-nearest-even."""
+    rng = np.random.default_rng(18)
+    inter = 96
+    g = rng.standard_normal((40, inter)) * 4
+    u = rng.standard_normal((40, inter))
+    G = np.concatenate([g, u], axis=1)  # float64, not bf16-representable
+    A = oracle.bf16_to_f64(oracle.swiglu_exact(G, inter))
+    want = _bf16_rne_f64(0.5 * g * (1.0 + np.tanh(0.5 * g)) * u)
+    assert (np.abs(A - want) <= 2.0**-8 * np.abs(want) + 1e-30).all()
+    assert (A == want).mean() > 0.999  # the two forms round alike except at rare ties
+    # rounding G to bf16 first (the separate-pass form) is a different result
+    A_rounded_first = oracle.bf16_to_f64(oracle.swiglu(oracle.bf16_from_f64(G), inter))
+    assert (A_rounded_first != A).mean() > 0.05
+    exact = g / (1.0 + np.exp(-g)) * u
+    assert np.abs(A - exact).mean() < np.abs(A_rounded_first - exact).mean()
+    # the up half scales the result exactly (power of two); SiLU(0) = 0; the gate
+    # half is the one that goes through SiLU (swapping the halves changes the result)
+    A2 = oracle.bf16_to_f64(oracle.swiglu_exact(np.concatenate([g, 2 * u], axis=1), inter))
+    np.testing.assert_array_equal(A2, 2 * A)
+    G3 = np.array([[0.0, -30.0, 5.0, 1.5, 5.0, -30.0]])
+    A3 = oracle.bf16_to_f64(oracle.swiglu_exact(G3, 3))[0]
+    assert A3[0] == 0.0
+    assert abs(A3[1]) < 1e-9  # SiLU(-30) * 5 ~ -4.7e-12
+    assert A3[2] == _bf16_rne_f64(np.array([5.0 / (1.0 + np.exp(-5.0)) * -30.0]))[0]
+
+
 def test_sampled_pipeline_agrees_with_full():
     w, r, vals, res = _tiny_full()
     toks = np.array([0, 5, 63, 17])
