@@ -282,13 +282,20 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *args,
  *
  * Behaviour:
  *  - n_local_experts > EP_MAX_LOCAL_EXPERTS or n_ranks > EP_MAX_RANKS: returns
- *    EP_ERR_UNSUPPORTED, nothing is enqueued.
- *  - The first call on a device looks up that device's address of the array
- *    (with the device current); make that first call before any stream capture.
+ *    EP_ERR_UNSUPPORTED, nothing is enqueued. Every check of
+ *    grouped_gemm_combine_send runs before anything is enqueued, so a call that
+ *    returns an error enqueues nothing.
+ *  - Each call outside stream capture looks up the current device's address of
+ *    the array (with that device current), so the address stays right after a
+ *    cudaDeviceReset. A call on a stream being captured uses the address found
+ *    by the last earlier call on that device: make the first call on a device
+ *    before any stream capture (else EP_ERR_CUDA).
  *  - Every call shares the array and it keeps the last call's contents, so each
  *    call first clears it with an asynchronous memset on `stream` (no allocation).
  *    Calls that overlap on the GPU (e.g. on two streams at once) race on the
  *    counters: issue them in order on one stream.
+ *  - overlap_previous gives no overlap here: the kernel launches behind that
+ *    memset, so it starts only after the previous work on `stream` has ended.
  *  - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
  * Everything else (arguments, results, signalling, status bits) is exactly as for
  * grouped_gemm_combine_send.

@@ -176,7 +176,13 @@ int ep_plan(const ep_config *cfg, const int32_t *topk_ids, const ep_plan_out *ou
     return cuda_status(ep::launch_plan(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_stream_t stream)
+}  // extern "C"
+
+namespace ep {
+
+// Every host check of grouped_gemm_combine_send, the tensor maps and the launch
+// parameters; nothing is enqueued.
+int prepare_send(const ep_config *cfg, const ep_send_args *a, PreparedSend *out)
 {
     int rc = check_config(cfg);
     if (rc != EP_OK)
@@ -298,18 +304,47 @@ int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_st
     const int64_t max_tiles = ((a->max_rows + ep::BM - 1) / ep::BM + El) * p.n_blocks;
     const int grid = static_cast<int>(max_tiles < num_sms ? (max_tiles < 1 ? 1 : max_tiles)
                                                           : num_sms);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     p.m_fastest = pick_m_fastest(rows_per_expert, pair ? 2 * ep::BM : ep::BM, p.n_blocks, cfg->K,
                                  cfg->N, elem, pair ? num_sms / 2 : grid) ? 1 : 0;
+    out->ta = ta;
+    out->tb = tb;
+    out->p = p;
+    out->bn = bn;
+    out->send_warps = cfg->send_warps;
+    out->grid = grid;
+    out->kind = pair ? PreparedSend::kPair : fp8 ? PreparedSend::kFp8 : PreparedSend::kBf16;
     if (pair) {
         const int64_t pair_tiles = ((a->max_rows + 2 * ep::BM - 1) / (2 * ep::BM) + El) * p.n_blocks;
-        const int max_pairs = static_cast<int>(
+        out->max_pairs = static_cast<int>(
             pair_tiles < num_sms / 2 ? (pair_tiles < 1 ? 1 : pair_tiles) : num_sms / 2);
-        return cuda_status(ep::launch_gemm_send_bf16_pair(ta, tb, p, max_pairs, s));
     }
-    return cuda_status(fp8 ? ep::launch_gemm_send_fp8(ta, tb, p, bn, grid, s)
-                           : ep::launch_gemm_send_bf16(ta, tb, p, bn, cfg->send_warps, grid,
-                                                       s));
+    return EP_OK;
+}
+
+int launch_prepared_send(const PreparedSend &ps, cudaStream_t s)
+{
+    switch (ps.kind) {
+    case PreparedSend::kPair:
+        return cuda_status(launch_gemm_send_bf16_pair(ps.ta, ps.tb, ps.p, ps.max_pairs, s));
+    case PreparedSend::kFp8:
+        return cuda_status(launch_gemm_send_fp8(ps.ta, ps.tb, ps.p, ps.bn, ps.grid, s));
+    default:
+        return cuda_status(
+            launch_gemm_send_bf16(ps.ta, ps.tb, ps.p, ps.bn, ps.send_warps, ps.grid, s));
+    }
+}
+
+}  // namespace ep
+
+extern "C" {
+
+int grouped_gemm_combine_send(const ep_config *cfg, const ep_send_args *a, ep_stream_t stream)
+{
+    ep::PreparedSend ps;
+    const int rc = ep::prepare_send(cfg, a, &ps);
+    if (rc != EP_OK)
+        return rc;
+    return ep::launch_prepared_send(ps, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ep_scatter_send(const ep_config *cfg, const ep_scatter_args *a, ep_stream_t stream)

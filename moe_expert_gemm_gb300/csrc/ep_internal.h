@@ -124,6 +124,18 @@ struct CombineParams {
     int overlap_previous;  // EP_OVERLAP_*: programmatic dependent of the previous kernel
 };
 
+// A checked grouped_gemm_combine_send call, ready to launch: prepare_send runs every
+// host check (returning EP_ERR_* with nothing enqueued), encodes the tensor maps and
+// picks the kernel; launch_prepared_send enqueues it (EP_OK or EP_ERR_CUDA).
+struct PreparedSend {
+    enum Kind { kBf16, kPair, kFp8 };
+    CUtensorMap ta, tb;
+    SendParams p;
+    int kind, bn, send_warps, grid, max_pairs;
+};
+int prepare_send(const ep_config *cfg, const ep_send_args *a, PreparedSend *out);
+int launch_prepared_send(const PreparedSend &ps, cudaStream_t s);
+
 // Kernel launchers; each returns the launch's cudaError_t.
 cudaError_t launch_plan(const PlanParams &p, cudaStream_t s);
 cudaError_t launch_gemm_send_bf16(const CUtensorMap &ta, const CUtensorMap &tb,
