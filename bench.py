@@ -50,7 +50,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_BYTES = 129 * 10**6
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
@@ -86,10 +86,15 @@ def parse_args():
     ap.add_argument("--send-warps", type=int, default=-1, choices=[-1, 0, 4],
                     help="sink placement: -1 library choice, 0 inside the output warps, "
                          "4 dedicated send warps (bf16)")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the per-workload measurements (every workload's rank 0 and "
+                         "most-loaded rank) that follow the headline at N=1")
+    ap.add_argument("--pw-steps", type=int, default=30,
+                    help="timed steps of each per-workload measurement")
     ap.add_argument("--solo", action="store_true",
                     help="profiling aid: only the timed rank's operands, no peer staging, and "
                          "the step is the fused send alone (no combine, no e2e, no baseline)")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -106,8 +111,106 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+class NvmlClocks:
+    """Read-only NVML queries (ctypes on the driver's libnvidia-ml) of one GPU's SM
+    clock, clock-event reasons and power: sampled every ~2 ms on a thread while a
+    timed region runs. Nothing is ever set."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int):
+        import ctypes
+        import threading
+        self.ct, self.threading = ctypes, threading
+        self.lib = self.handle = None
+        self.samples = []
+        self.thread = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            self.lib = lib
+            self.handle = self._find_handle(device_index)
+        except (OSError, AttributeError):
+            self.lib = None
+        if self.handle is None:
+            self.lib = None
+        else:
+            reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            self.reasons_fn = reasons or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _find_handle(self, device_index: int):
+        import torch
+        ct = self.ct
+        props = torch.cuda.get_device_properties(device_index)
+        h = ct.c_void_p()
+        uuid = getattr(props, "uuid", None)
+        if uuid is not None:
+            u = str(uuid)
+            u = u if u.startswith("GPU-") else "GPU-" + u
+            if self.lib.nvmlDeviceGetHandleByUUID(u.encode(), ct.byref(h)) == 0:
+                return h
+        if hasattr(props, "pci_bus_id"):
+            bus = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                        props.pci_device_id)
+            if self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ct.byref(h)) == 0:
+                return h
+        return None
+
+    @property
+    def ok(self) -> bool:
+        return self.lib is not None
+
+    def read(self):
+        ct = self.ct
+        mhz, reasons, mw = ct.c_uint(0), ct.c_ulonglong(0), ct.c_uint(0)
+        self.lib.nvmlDeviceGetClockInfo(self.handle, 1, ct.byref(mhz))  # NVML_CLOCK_SM
+        self.reasons_fn(self.handle, ct.byref(reasons))
+        self.lib.nvmlDeviceGetPowerUsage(self.handle, ct.byref(mw))
+        return time.perf_counter(), mhz.value, reasons.value, mw.value / 1e3
+
+    def max_sm_mhz(self):
+        v = self.ct.c_uint(0)
+        self.lib.nvmlDeviceGetMaxClockInfo(self.handle, 1, self.ct.byref(v))
+        return v.value
+
+    def start(self):
+        if not self.ok:
+            return
+        self.samples = []
+        self.stop_flag = False
+
+        def loop():
+            while not self.stop_flag:
+                self.samples.append(self.read())
+                time.sleep(0.002)
+        self.thread = self.threading.Thread(target=loop, daemon=True)
+        self.thread.start()
+
+    def stop(self, busy=None):
+        """Summary of the samples; ``busy`` (t0, t1) perf_counter bounds keep only the
+        samples taken while the GPU was known to be running the timed work."""
+        if not self.ok or self.thread is None:
+            return None
+        self.stop_flag = True
+        self.thread.join()
+        rows = self.samples
+        if busy is not None:
+            rows = [r for r in rows if busy[0] <= r[0] <= busy[1]] or rows
+        if not rows:
+            return None
+        reasons = sorted({name for r in rows for bit, name in self.REASONS.items()
+                          if r[2] & bit})
+        return {"sm_mhz": statistics.median(r[1] for r in rows),
+                "sm_mhz_min": min(r[1] for r in rows), "sm_max_mhz": self.max_sm_mhz(),
+                "power_w_max": max(r[3] for r in rows), "reasons": reasons,
+                "samples": len(rows), "source": "NVML, read-only, every ~2 ms in-process"}
+
+
 class ClockSampler:
-    """nvidia-smi sampling (100 ms) of SM clocks and throttle reasons."""
+    """nvidia-smi sampling (100 ms) of SM clocks and throttle reasons: the fallback
+    when NVML cannot be loaded in-process."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -130,7 +233,7 @@ class ClockSampler:
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self):
+    def stop(self, busy=None):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -154,7 +257,12 @@ class ClockSampler:
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
-                "samples": len(rows)}
+                "samples": len(rows), "source": "nvidia-smi every 100 ms"}
+
+
+def clock_sampler(device_index: int):
+    s = NvmlClocks(device_index)
+    return s if s.ok else ClockSampler(device_index)
 
 
 # Sources that decide what the fused GEMM+send kernels do on the device: the kernels,
@@ -207,6 +315,151 @@ def algorithmic_work(w, plan_counts: np.ndarray, m_rows: int):
         send_bytes += m_rows * (w.K // 128) * 4 + nonempty * (w.N // 128) * (w.K // 128) * 4
     comb_bytes = w.tokens * w.top_k * w.N * 2 + w.tokens * w.N * 2 + w.tokens * w.top_k * 4
     return flops, float(send_bytes), float(comb_bytes)
+
+
+def l2_policy(w, rows_q: int) -> tuple[bool, str]:
+    """Whether every step flushes L2, and the config text saying so: the step's
+    operand bytes (A of the timed rank and its experts' W) against twice the L2."""
+    elem = 1 if w.dtype == "fp8_1d2d" else 2
+    step_bytes = rows_q * w.K * elem + w.n_local_experts * w.N * w.K * elem
+    if step_bytes < 2 * L2_BYTES:
+        return True, "flushed with a 512 MB write before every step"
+    return False, f"per-step inputs {step_bytes / 1e6:.0f} MB > L2"
+
+
+def config_dict(w, q: int, rows_q: int, args, world: int) -> dict:
+    """The workload description both arms print (same keys, same values)."""
+    return {"workload": w.name, "n_ranks": w.n_ranks, "n_local_experts": w.n_local_experts,
+            "top_k": w.top_k, "tokens_per_rank": w.tokens, "K": w.K, "N": w.N,
+            "operands": w.dtype, "my_rank": q, "rows": int(rows_q),
+            "send_warps": args.send_warps, "path": args.path,
+            "combine_overlaps_send": bool(args.overlap and args.path != "unfused"),
+            "signal_mode": args.signal_mode, "l2": l2_policy(w, rows_q)[1],
+            "parallelism": "replicas: one logical rank per GPU" if world > 1
+            else "one logical rank"}
+
+
+def roofline(w, flops: float, nbytes: float, dom_s: float, peaks: dict, peak_src: str,
+             traffic=None) -> dict:
+    """Roofline entry of one kernel: tensor-bound when its FLOPs at the tensor peak
+    take longer than its bytes at the HBM peak, else HBM-bound."""
+    peak_tf = float(peaks["bf16_tflops"]) * (2.0 if w.dtype == "fp8_1d2d" else 1.0)
+    peak_bw = float(peaks["hbm_gbs"])
+    if flops / (peak_tf * 1e12) >= nbytes / (peak_bw * 1e9):
+        tf = flops / dom_s / 1e12
+        roof = {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": tf / peak_tf, "traffic": traffic}
+    else:
+        gbs = nbytes / dom_s / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peak_bw, "unit": "GB/s",
+                "frac": gbs / peak_bw, "traffic": traffic}
+    roof["peak_source"] = (f"{peak_src}: " + ("bf16_tflops (burst)" if roof["bound"] == "tensor"
+                                              else "hbm_gbs")
+                           + (" x2 nominal fp8/bf16 ratio" if w.dtype == "fp8_1d2d"
+                              and roof["bound"] == "tensor" else ""))
+    return roof
+
+
+def measure_workload(name: str, steps: int, warmup: int, peaks: dict, peak_src: str,
+                     device_index: int, probe_s: float = 0.5) -> dict:
+    """Fused send and combine of rank 0 and of the most-loaded rank of one workload,
+    every rank staged as in the headline step (serialised kernels, CUDA events on the
+    launching stream, L2 flushed between steps where the inputs fit in it), then a
+    back-to-back probe of the same step under NVML clock sampling."""
+    import torch
+    from moe_expert_gemm_gb300.system import EpSystem
+    from synth import WORKLOADS, make_rank_values, make_routing, rows_per_rank
+
+    w = WORKLOADS[name]
+    routing = make_routing(w)
+    rows = rows_per_rank(w, routing.topk_ids)
+    qmax = int(np.argmax(rows))
+    targets = [0] if qmax == 0 else [0, qmax]
+    s = EpSystem(w.n_ranks, w.n_local_experts, w.top_k, w.tokens, w.K, w.N, w.dtype)
+    s.set_routing(routing.topk_ids)
+    for r in range(w.n_ranks):
+        s.plan(r)
+        v = make_rank_values(w, r, int(rows[r]))
+        s.set_operands(r, v["A"], v["W"], v.get("a_scales"), v.get("w_scales"))
+        del v
+    for q in targets:
+        s.set_gates(q, routing.gates[q])
+    for r in range(w.n_ranks):
+        s.send(r, epoch=1)
+    torch.cuda.synchronize()
+    if s.status_words().any():
+        raise SystemExit(f"{name}: device status after staging: {s.status_words()}")
+    stream = torch.cuda.current_stream()
+    epoch = [2]
+    out = {}
+    for q in targets:
+        peer_idx = torch.tensor([w.n_local_experts * w.n_ranks + r for r in range(w.n_ranks)
+                                 if r != q], dtype=torch.int64, device="cuda")
+        plan_q = s.plan_host(q)
+        m_rows = plan_q["m_total"]
+        flops, send_bytes, comb_bytes = algorithmic_work(w, plan_q["send_counts"], m_rows)
+        need_flush, l2_text = l2_policy(w, m_rows)
+        flush = torch.empty(512 * 2**20, dtype=torch.uint8, device="cuda") if need_flush else None
+
+        def step(ev=None):
+            e = epoch[0]
+            epoch[0] += 1
+            if flush is not None:
+                flush.fill_(e & 0xFF)
+            if peer_idx.numel():
+                s.counts[q].index_fill_(0, peer_idx, e)
+            if ev is not None:
+                ev[0].record(stream)
+            s.send(q, e, stream)
+            if ev is not None:
+                ev[1].record(stream)
+            s.combine(q, e, stream)
+            if ev is not None:
+                ev[2].record(stream)
+
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        for i in range(steps):
+            step(evs[i])
+        torch.cuda.synchronize()
+        send_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+        comb_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+        # the same step back to back for ~probe_s, under clock sampling
+        clk = clock_sampler(device_index)
+        clk.start()
+        probe = []
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < probe_s and len(probe) < 20000:
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            step(ev)
+            probe.append(ev)
+            if len(probe) % 64 == 0:
+                probe[-64][2].synchronize()  # keep the queue short
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        clocks = clk.stop(busy=(t0, t1))
+        probe_send = statistics.mean(e[0].elapsed_time(e[1]) for e in probe)
+        if s.status_words().any():
+            raise SystemExit(f"{name}: device status after timing: {s.status_words()}")
+        roof = roofline(w, flops, send_bytes, send_ms / 1e3, peaks, peak_src,
+                        measured_traffic(w.name, "grouped_gemm_combine_send") if q == 0 else None)
+        entry = {"rank": q, "rows": int(m_rows), "steps": steps, "warmup": warmup,
+                 "fused_ms": send_ms, "combine_ms": comb_ms, "step_ms": send_ms + comb_ms,
+                 "tokens_per_s": w.tokens / ((send_ms + comb_ms) / 1e3),
+                 "tflops": flops / (send_ms / 1e3) / 1e12,
+                 "combine_gbs": comb_bytes / (comb_ms / 1e3) / 1e9,
+                 "roofline": roof, "l2": l2_text,
+                 "probe": {"seconds": t1 - t0, "steps": len(probe), "fused_ms": probe_send,
+                           "clocks": clocks}}
+        if clocks and clocks.get("sm_mhz"):
+            entry["probe"]["fused_kcycles_at_median_clock"] = probe_send * clocks["sm_mhz"]
+        out["rank0" if q == 0 else "max_rank"] = entry
+        del flush
+    del s
+    torch.cuda.empty_cache()
+    return out
 
 
 # ----------------------------------------------------------------- oracle arm
@@ -306,9 +559,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "n_ranks": w.n_ranks,
-                       "n_local_experts": w.n_local_experts, "top_k": w.top_k,
-                       "tokens_per_rank": w.tokens, "K": w.K, "N": w.N, "my_rank": q},
+            "config": config_dict(w, q, int(rows[q]), args, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -403,8 +654,8 @@ def main():
             s.counts[q].index_fill_(0, peer_idx, e)
     step_bytes = int(s.ops[q]["A"].numel() * s.ops[q]["A"].element_size()
                      + s.ops[q]["W"].numel() * s.ops[q]["W"].element_size())
-    flush = torch.empty(512 * 2**20, dtype=torch.uint8, device="cuda") \
-        if step_bytes < 2 * L2_BYTES else None
+    need_flush = step_bytes < 2 * L2_BYTES if layer else l2_policy(w, m_rows)[0]
+    flush = torch.empty(512 * 2**20, dtype=torch.uint8, device="cuda") if need_flush else None
     epoch = [2]
     unfused = args.path == "unfused"
     C_local = s.local_C(q) if unfused else None
@@ -448,27 +699,29 @@ def main():
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    clocks = ClockSampler(torch.cuda.current_device())
+    clocks = clock_sampler(torch.cuda.current_device())
     clocks.start()
-    time.sleep(0.5)  # let the sampler start before the timed region
+    time.sleep(0.05 if isinstance(clocks, NvmlClocks) else 0.5)  # sampler running first
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
     # with overlap, every timed step is followed by the same step with its kernels
     # serialised, which gives the per-kernel times under the same clocks and power
     serial_events = ([[torch.cuda.Event(enable_timing=True) for _ in range(8)]
                       for _ in range(args.steps)] if overlap else None)
     torch.cuda.synchronize()
+    t_busy0 = time.perf_counter()
     for i in range(args.steps):
         one_step(events[i])
         if overlap:
             one_step(serial_events[i], serial=True)
     torch.cuda.synchronize()
+    t_busy1 = time.perf_counter()
     if world > 1:
         dist.barrier()
     step_overlapped = (statistics.mean(e[0].elapsed_time(e[2]) for e in events)
                        if overlap else None)
     if overlap:
         events = serial_events
-    clk = clocks.stop()
+    clk = clocks.stop(busy=(t_busy0, t_busy1))
     send_ms = [e[0].elapsed_time(e[1]) for e in events]
     comb_ms = [e[1].elapsed_time(e[2]) for e in events]
     gemm_ms = [e[0].elapsed_time(e[3]) for e in events] if unfused else None
@@ -591,25 +844,11 @@ def main():
     else:
         dom_s = statistics.mean(gemm_ms) / 1e3 if unfused else send_s
     tflops = flops / dom_s / 1e12
-    peak_tf = float(peaks["bf16_tflops"]) * (2.0 if w.dtype == "fp8_1d2d" else 1.0)
-    peak_bw = float(peaks["hbm_gbs"])
-    t_tensor = flops / (peak_tf * 1e12)
-    t_hbm = send_bytes / (peak_bw * 1e9)
     traffic = None if unfused or layer else measured_traffic(w.name, "grouped_gemm_combine_send")
-    if t_tensor >= t_hbm:
-        roof = {"bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": tflops / peak_tf, "traffic": traffic}
-    else:
-        gbs = send_bytes / dom_s / 1e9
-        roof = {"bound": "hbm", "achieved": gbs, "peak": peak_bw, "unit": "GB/s",
-                "frac": gbs / peak_bw, "traffic": traffic}
+    roof = roofline(w, flops, send_bytes, dom_s, peaks, peak_src, traffic)
     roof["kernel"] = ("grouped_gemm_combine_send with the sink disabled (rows to a local C)"
                       if unfused else "the up/gate grouped GEMM (K = H, N = 2I, rows to a "
                       "local buffer)" if layer else "grouped_gemm_combine_send")
-    roof["peak_source"] = (f"{peak_src}: " + ("bf16_tflops (burst)" if roof["bound"] == "tensor"
-                                              else "hbm_gbs")
-                           + (" x2 nominal fp8/bf16 ratio" if w.dtype == "fp8_1d2d"
-                              and roof["bound"] == "tensor" else ""))
     roof["algorithmic_per_launch"] = {"flops": flops, "bytes": send_bytes}
 
     line = {
@@ -618,16 +857,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "e4m3",
         "data": "synthetic (seeded; shapes and laws of the named workload)",
-        "config": {"workload": w.name, "n_ranks": w.n_ranks, "n_local_experts": w.n_local_experts,
-                   "top_k": w.top_k, "tokens_per_rank": w.tokens, "K": w.K, "N": w.N,
-                   "operands": w.dtype, "my_rank": q, "rows": m_rows,
-                   "send_warps": args.send_warps, "path": args.path,
-                   "combine_overlaps_send": overlap,
-                   "signal_mode": args.signal_mode,
-                   "l2": ("flushed with a 512 MB write before every step" if flush is not None
-                          else f"per-step inputs {step_bytes / 1e6:.0f} MB > L2"),
-                   "parallelism": "replicas: one logical rank per GPU" if world > 1
-                   else "one logical rank"},
+        "config": config_dict(w, q, m_rows, args, world),
         "tflops": tflops,
         "kernels_ms": ({"ep_dispatch_gather": stage_ms[0],
                         "up/gate grouped_gemm_combine_send (local buffer)": stage_ms[1],
@@ -651,9 +881,23 @@ def main():
     if args.solo:
         line["config"]["solo"] = "profiling aid: fused send only, peers not staged"
     if layer:
+        line["config"]["l2"] = ("flushed with a 512 MB write before every step" if need_flush
+                                else f"per-step inputs {step_bytes / 1e6:.0f} MB > L2")
         line["config"]["layer"] = {"hidden": w.N, "intermediate": w.K,
                                    "activation": args.layer_act,
                                    "metric": "tokens/s of the whole layer for one rank"}
+    if (rank == 0 and world == 1 and not args.no_per_workload and not args.solo
+            and args.path == "fused" and not overlap and args.signal_mode == "rank_flag"
+            and args.tokens is None and args.send_warps == -1):
+        # every workload's fused send and combine (rank 0 and the most-loaded rank),
+        # measured in this process after the headline
+        del s, C_local
+        torch.cuda.empty_cache()
+        pw = {}
+        for name in WORKLOADS:
+            pw[name] = measure_workload(name, args.pw_steps, max(3, min(args.warmup, 5)),
+                                        peaks, peak_src, torch.cuda.current_device())
+        line["per_workload"] = pw
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.solo and not layer:
         import oracle
         plans = {r: oracle.plan(w.n_ranks, w.n_local_experts, w.top_k, routing.topk_ids, r)

@@ -75,18 +75,24 @@ def test_single_process_helpers():
 def test_reference_arm_line_on_rank_0():
     """The reference arm's JSON line (the oracle on the host, tiny workload): the keys
     the driver reads, its cpu_baseline describing the run, and an e2e equal to it."""
-    import argparse
     import json
     sys.path.insert(0, ROOT)
     import bench
     out = io.StringIO()
     with redirect_stdout(out):
-        bench.run_reference(argparse.Namespace(workload="tiny", steps=2, warmup=1, rank="1"), 0, 1)
+        args = bench.parse_args(["--impl", "reference", "--workload", "tiny", "--steps", "2",
+                                 "--warmup", "1", "--rank", "1"])
+        bench.run_reference(args, 0, 1)
     line = json.loads(out.getvalue().strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "tokens/s"
     assert line["steps"] == 2 and line["warmup"] == 1 and line["n_gpus"] == 1
     assert line["higher_is_better"] is True and line["value"] > 0
     assert line["config"]["workload"] == "tiny" and line["config"]["my_rank"] == 1
+    # the same config the GPU arm prints for these arguments, key for key
+    from synth import WORKLOADS, make_routing, rows_per_rank
+    w = WORKLOADS["tiny"]
+    rows = rows_per_rank(w, make_routing(w).topk_ids)
+    assert line["config"] == bench.config_dict(w, 1, int(rows[1]), args, 1)
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
     assert "rank 1" in cb["sample"]
