@@ -445,6 +445,47 @@ typedef struct {
 
 int ep_combine_reduce(const ep_config *cfg, const ep_combine_args *args, ep_stream_t stream);
 
+/* ------------------------------------------------- peers in other processes */
+
+/*
+ * Sharing receive buffers between the processes of an expert-parallel group on one
+ * node, one rank per process. "ep_signal_completion" sends by direct memory access
+ * when the target device is on the same node, and "P3PeerSendConfig" holds one
+ * receive-buffer pointer per rank (recv_buf_ptrs): each rank exports the buffers
+ * its peers write (its receive buffer and its receive-count buffer), every other
+ * rank imports them and passes the imported pointers in ep_send_args.recv_buf_ptrs /
+ * recv_count_ptrs. The kernels then store rows, count words and flags there exactly
+ * as into local buffers (plain stores, system-scope releases). Carrying the handle
+ * bytes from process to process is the caller's business (any host channel).
+ *
+ * ep_ipc_export  dev_ptr: a device buffer of the calling process, allocated with
+ *                cudaMalloc (directly, or inside a block of a caching allocator; not
+ *                VMM or stream-ordered pool memory). Fills *out with a CUDA IPC handle
+ *                of the allocation holding it, dev_ptr's offset in that allocation
+ *                and the bytes from dev_ptr to the allocation's end.
+ *                EP_ERR_INVALID_ARG for NULL or a pointer that is not device memory
+ *                of the current context; EP_ERR_CUDA if the runtime refuses a handle.
+ * ep_ipc_import  maps an exported buffer of another process into this one (on the
+ *                current device; peer access is enabled when that is another GPU)
+ *                and returns its address in *dev_ptr. A process cannot import its own
+ *                handles. EP_ERR_CUDA if the runtime refuses.
+ * ep_ipc_close   unmaps a buffer ep_ipc_import mapped (same handle and address).
+ * The exporting process must keep the buffer allocated until every importer has
+ * closed it: a store into a buffer whose owner freed it is an invalid access.
+ * These three calls are synchronous host calls (no stream).
+ */
+#define EP_IPC_HANDLE_BYTES 64
+
+typedef struct {
+    uint8_t handle[EP_IPC_HANDLE_BYTES];
+    uint64_t offset;
+    uint64_t bytes;
+} ep_ipc_handle;
+
+int ep_ipc_export(const void *dev_ptr, ep_ipc_handle *out);
+int ep_ipc_import(const ep_ipc_handle *h, void **dev_ptr);
+int ep_ipc_close(const ep_ipc_handle *h, void *dev_ptr);
+
 /* Static description of a return code or status bit set. */
 const char *ep_strerror(int code);
 

@@ -87,6 +87,14 @@ class ep_swiglu_args(ctypes.Structure):
                 ("inter", _c_i32)]
 
 
+EP_IPC_HANDLE_BYTES = 64
+
+
+class ep_ipc_handle(ctypes.Structure):
+    _fields_ = [("handle", ctypes.c_uint8 * EP_IPC_HANDLE_BYTES), ("offset", _c_u64),
+                ("bytes", _c_u64)]
+
+
 class EpError(RuntimeError):
     def __init__(self, code: int, where: str):
         super().__init__(f"{where}: {ep_strerror(code)} ({code})")
@@ -97,7 +105,7 @@ _lib = None
 
 EXPORTS = ("ep_plan_sizes", "ep_plan", "grouped_gemm_combine_send", "ep_combine_reduce",
            "ep_strerror", "grouped_gemm_combine_send_noalloc", "ep_scatter_send",
-           "ep_dispatch_gather", "ep_swiglu")
+           "ep_dispatch_gather", "ep_swiglu", "ep_ipc_export", "ep_ipc_import", "ep_ipc_close")
 
 
 def load(build_if_missing: bool = True):
@@ -122,9 +130,12 @@ def load(build_if_missing: bool = True):
     L.ep_dispatch_gather.argtypes = [ctypes.POINTER(ep_config), ctypes.POINTER(ep_dispatch_args),
                                      _vp]
     L.ep_swiglu.argtypes = [ctypes.POINTER(ep_config), ctypes.POINTER(ep_swiglu_args), _vp]
+    L.ep_ipc_export.argtypes = [_vp, ctypes.POINTER(ep_ipc_handle)]
+    L.ep_ipc_import.argtypes = [ctypes.POINTER(ep_ipc_handle), ctypes.POINTER(_vp)]
+    L.ep_ipc_close.argtypes = [ctypes.POINTER(ep_ipc_handle), _vp]
     for f in ("ep_plan_sizes", "ep_plan", "grouped_gemm_combine_send", "ep_combine_reduce",
               "grouped_gemm_combine_send_noalloc", "ep_scatter_send", "ep_dispatch_gather",
-              "ep_swiglu"):
+              "ep_swiglu", "ep_ipc_export", "ep_ipc_import", "ep_ipc_close"):
         getattr(L, f).restype = ctypes.c_int
     L.ep_strerror.argtypes = [ctypes.c_int]
     L.ep_strerror.restype = ctypes.c_char_p
@@ -206,6 +217,25 @@ def ep_swiglu(cfg: ep_config, args: ep_swiglu_args, stream=None) -> int:
 def ep_combine_reduce(cfg: ep_config, args: ep_combine_args, stream=None) -> int:
     return _check(load().ep_combine_reduce(ctypes.byref(cfg), ctypes.byref(args),
                                            stream_handle(stream)), "ep_combine_reduce")
+
+
+def ep_ipc_export(dev_ptr) -> ep_ipc_handle:
+    """CUDA IPC handle (plus offset) of a device buffer of this process, for the peer
+    processes of an expert-parallel group to map (ep_ipc_import)."""
+    h = ep_ipc_handle()
+    _check(load().ep_ipc_export(ptr(dev_ptr), ctypes.byref(h)), "ep_ipc_export")
+    return h
+
+
+def ep_ipc_import(h: ep_ipc_handle) -> int:
+    """Map another process's exported buffer; returns its address in this process."""
+    out = _vp(0)
+    _check(load().ep_ipc_import(ctypes.byref(h), ctypes.byref(out)), "ep_ipc_import")
+    return int(out.value)
+
+
+def ep_ipc_close(h: ep_ipc_handle, dev_ptr: int) -> int:
+    return _check(load().ep_ipc_close(ctypes.byref(h), ptr(dev_ptr)), "ep_ipc_close")
 
 
 def raw_call(name: str, *args) -> int:

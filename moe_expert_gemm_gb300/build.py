@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(OUT_DIR, "libmoe_ep.so")
 
 SOURCES = ["ep_api.cu", "ep_plan.cu", "ep_gemm_send.cu", "ep_gemm_send_fp8.cu",
            "ep_gemm_send_pair.cu", "ep_combine.cu",
-           "ep_noalloc.cu", "ep_scatter.cu", "ep_layer.cu"]
+           "ep_noalloc.cu", "ep_scatter.cu", "ep_layer.cu", "ep_ipc.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

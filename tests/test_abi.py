@@ -186,6 +186,13 @@ def test_combine_overlap_mode_is_checked(lib):
         ep.EP_ERR_INVALID_ARG
 
 
+def test_ipc_calls_reject_null_arguments(lib):
+    h = ep.ep_ipc_handle()
+    assert ep.raw_call("ep_ipc_export", None, ctypes.byref(h)) == ep.EP_ERR_INVALID_ARG
+    assert ep.raw_call("ep_ipc_import", None, None) == ep.EP_ERR_INVALID_ARG
+    assert ep.raw_call("ep_ipc_close", ctypes.byref(h), None) == ep.EP_ERR_INVALID_ARG
+
+
 def test_strerror(lib):
     assert ep.ep_strerror(ep.EP_ERR_UNSUPPORTED) == "unsupported configuration"
     assert "timed out" in ep.ep_strerror(ep.EP_STATUS_TIMEOUT)
@@ -200,7 +207,7 @@ def test_binding_structs_match_the_header(tmp_path):
     if cc is None:
         pytest.skip("no C compiler")
     structs = [ep.ep_config, ep.ep_plan_out, ep.ep_send_args, ep.ep_combine_args,
-               ep.ep_scatter_args, ep.ep_dispatch_args, ep.ep_swiglu_args]
+               ep.ep_scatter_args, ep.ep_dispatch_args, ep.ep_swiglu_args, ep.ep_ipc_handle]
     lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "moe_ep.h"', "int main(void) {"]
     for cls in structs:
         name = cls.__name__

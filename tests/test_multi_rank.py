@@ -98,3 +98,66 @@ def test_reference_arm_line_on_rank_0():
     assert "rank 1" in cb["sample"]
     assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def _ipc_worker(rank, world, port, q):
+    """Handle exchange of the one-rank-per-process path over gloo, with stand-in
+    handles and a stand-in import (no GPU): each rank's table holds its own
+    addresses at its own index and what it imported from every peer elsewhere."""
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import torch.distributed as dist
+    from moe_expert_gemm_gb300 import ep_ipc_handle
+    from moe_expert_gemm_gb300.peers import handle_bytes, handle_from_bytes, peer_tables
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        mine = []
+        for kind in range(2):  # receive buffer, receive-count buffer
+            h = ep_ipc_handle()
+            h.handle[0], h.handle[63] = rank, kind
+            h.offset, h.bytes = 4096 * (rank + 1) + kind, 1 << 20
+            mine.append(handle_bytes(h))
+        gathered = [None] * world
+        dist.all_gather_object(gathered, tuple(mine))
+        imported = []
+
+        def fake_import(b):
+            h = handle_from_bytes(b)
+            imported.append((h.handle[0], h.handle[63], h.offset))
+            return 10_000 * (h.handle[0] + 1) + 100 * h.handle[63] + h.offset % 4096
+        own = (111 + rank, 222 + rank)
+        tables = peer_tables(rank, own, gathered, fake_import)
+        q.put(dict(rank=rank, tables=tables, imported=sorted(imported)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_ipc_handle_exchange_over_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29800 + os.getpid() % 1000
+    procs = [ctx.Process(target=_ipc_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted((q.get(timeout=120) for _ in procs), key=lambda d: d["rank"])
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    # rank 0: its own buffers at index 0, rank 1's imported (kind k -> 20000 + 100k + k)
+    assert res[0]["tables"] == [[111, 20_000 + 0 + 0], [222, 20_000 + 100 + 1]]
+    assert res[1]["tables"] == [[10_000 + 0 + 0, 112], [10_000 + 100 + 1, 223]]
+    # each rank imported exactly its peer's two handles, with their offsets
+    assert res[0]["imported"] == [(1, 0, 8192), (1, 1, 8193)]
+    assert res[1]["imported"] == [(0, 0, 4096), (0, 1, 4097)]
+
+
+def test_peer_tables_reject_mismatched_exports():
+    import pytest
+    sys.path.insert(0, ROOT)
+    from moe_expert_gemm_gb300.peers import handle_from_bytes, peer_tables
+    with pytest.raises(ValueError):
+        peer_tables(2, (1, 2), [(b"a", b"b"), (b"c", b"d")], lambda b: 0)
+    with pytest.raises(ValueError):
+        peer_tables(0, (1, 2), [(b"a", b"b"), (b"c",)], lambda b: 0)
+    with pytest.raises(ValueError):
+        handle_from_bytes(b"short")
