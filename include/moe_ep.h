@@ -89,9 +89,9 @@ typedef struct CUstream_st *ep_stream_t;
  *                        ("EpiloguePeerSink" SendWarps): 0 runs the send inside the
  *                        output warps; 4 adds four send warps, one per output warp,
  *                        that store the rows the output warps stage (bf16 only, on
- *                        single CTAs; fp8 gives EP_ERR_UNSUPPORTED); -1 lets the
- *                        library choose (today: inside the output warps). Any other
- *                        value gives EP_ERR_INVALID_ARG.
+ *                        single CTAs and on CTA pairs; fp8 gives EP_ERR_UNSUPPORTED);
+ *                        -1 lets the library choose (today: inside the output
+ *                        warps). Any other value gives EP_ERR_INVALID_ARG.
  *   signal_mode          EP_SIGNAL_RANK_FLAG or EP_SIGNAL_PER_EXPERT; producers and
  *                        consumers of one exchange must use the same mode.
  */

@@ -248,12 +248,10 @@ int prepare_send(const ep_config *cfg, const ep_send_args *a, PreparedSend *out)
     // an expert's expected rows, T*top_k/E_l, fill a 256-row pair tile; with fewer rows
     // (decode) the pair's extra padded MMA rows cost more than the traffic saved. The
     // fp8 kernel stays on single CTAs: its per-K-block hand-off of partial buffers
-    // between MMA and promotion would cross the pair every K block. Dedicated send
-    // warps (send_warps = 4) exist in the single-CTA kernel only.
+    // between MMA and promotion would cross the pair every K block.
     const int64_t rows_per_expert =
         static_cast<int64_t>(cfg->num_tokens) * cfg->top_k / cfg->n_local_experts;
-    const bool pair =
-        !fp8 && bn == 256 && rows_per_expert >= 2 * ep::BM && cfg->send_warps != 4;
+    const bool pair = !fp8 && bn == 256 && rows_per_expert >= 2 * ep::BM;
     CUtensorMap ta, tb;
     if (!encode_2d(&ta, dt, a->A, cfg->K, a->max_rows, static_cast<uint64_t>(cfg->K) * elem,
                    box_k, ep::BM))
@@ -325,7 +323,8 @@ int launch_prepared_send(const PreparedSend &ps, cudaStream_t s)
 {
     switch (ps.kind) {
     case PreparedSend::kPair:
-        return cuda_status(launch_gemm_send_bf16_pair(ps.ta, ps.tb, ps.p, ps.max_pairs, s));
+        return cuda_status(
+            launch_gemm_send_bf16_pair(ps.ta, ps.tb, ps.p, ps.send_warps, ps.max_pairs, s));
     case PreparedSend::kFp8:
         return cuda_status(launch_gemm_send_fp8(ps.ta, ps.tb, ps.p, ps.bn, ps.grid, s));
     default:

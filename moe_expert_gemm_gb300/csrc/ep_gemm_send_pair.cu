@@ -21,6 +21,11 @@
 //    one before the TMEM is freed (no MMA still writing the peer's TMEM).
 // All waits except these two cluster barriers are bounded; every role reaches
 // the final cluster barrier on every path.
+//
+// SEND = 4 adds four send warps (7-10), one per output warp, that store the rows
+// the output warps stage in two slots each ("EpiloguePeerSink" SendWarps: the
+// output warps go back to reading the accumulator while the previous 64 columns
+// leave); the second slot takes the room of one operand stage.
 #include <cuda_bf16.h>
 
 #include "ep_internal.h"
@@ -29,35 +34,51 @@
 
 namespace ep {
 
+// A staging slot's row destinations, handed with the slot from an output warp to its
+// send warp (SEND = 4).
+struct PairSlotMeta {
+    unsigned long long row_base[32];
+    int col_byte;
+    int pad[3];
+};
+
+template <int SEND>
 struct PairLayout {
     static constexpr int BN = 256;
-    static constexpr int STAGES = 6;
+    static constexpr int STAGES = SEND ? 5 : 6;
     static constexpr int kAccStages = 2;              // TMEM accumulators per CTA
     static constexpr int kTileRows = 2 * BM;          // rows of a pair tile
     static constexpr int kABytes = BM * kRowBytesK;   // this CTA's 128 rows of A
     static constexpr int kBBytes = (BN / 2) * kRowBytesK;  // this CTA's half of the W block
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kEpiWarps = 4;
-    static constexpr int kWarpStaging = 32 * 128;
+    static constexpr int kSlots = SEND ? 2 : 1;    // staging slots per output warp
+    static constexpr int kWarpStaging = 32 * 128;  // 32 rows x 64 bf16 columns
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + STAGES * kABytes;
     static constexpr int kOffStaging = kOffB + STAGES * kBBytes;
-    static constexpr int kOffBars = kOffStaging + kEpiWarps * kWarpStaging;
-    static constexpr int kNumBars = 2 * STAGES + 5;
+    static constexpr int kOffMeta = kOffStaging + kEpiWarps * kSlots * kWarpStaging;
+    static constexpr int kOffBars =
+        kOffMeta + (SEND ? kEpiWarps * kSlots * static_cast<int>(sizeof(PairSlotMeta)) : 0);
+    // full, empty, acc_full x2, acc_empty x2, mma_done (+ slot_full, slot_empty per slot)
+    static constexpr int kNumBars = 2 * STAGES + 5 + (SEND ? 2 * kEpiWarps * kSlots : 0);
     static constexpr int kOffSink = (kOffBars + kNumBars * 8 + 15) / 16 * 16;
     static constexpr int kEnd = kOffSink + static_cast<int>(sizeof(SinkShared));
     static constexpr int kSmemBytes = kEnd + 1024;
     static constexpr uint32_t kTmemCols = kAccStages * BN;
-    static constexpr int kThreads = 224;
+    // TMA, MMA, 4 output warps, completion (+ send warps)
+    static constexpr int kThreads = 224 + 32 * SEND;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(SEND == 0 || SEND == kEpiWarps, "send warps: none, or one per output warp");
 };
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
+template <int SEND>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224 + 32 * SEND, 1)
     gemm_send_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                const __grid_constant__ CUtensorMap tmap_b,
                                const __grid_constant__ SendParams p)
 {
-    using L = PairLayout;
+    using L = PairLayout<SEND>;
     constexpr int BN = L::BN;
     constexpr int STAGES = L::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -74,6 +95,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
     uint64_t *acc_full = bars + 2 * STAGES;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *mma_done = acc_empty + 2;
+    uint64_t *slot_full = mma_done + 1;  // [output warp][slot], SEND only
+    uint64_t *slot_empty = slot_full + L::kEpiWarps * L::kSlots;
+    PairSlotMeta *meta = reinterpret_cast<PairSlotMeta *>(smem + L::kOffMeta);
     SinkShared *sh = reinterpret_cast<SinkShared *>(smem + L::kOffSink);
     volatile int *abort_flag = &sh->abort_flag;
     const int El = p.El;
@@ -88,6 +112,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
             mbar_init(&acc_empty[a], 2 * L::kEpiWarps);  // both CTAs' epilogue warps
         }
         mbar_init(mma_done, 1);
+        if (SEND) {
+            for (int j = 0; j < L::kEpiWarps * L::kSlots; ++j) {
+                mbar_init(&slot_full[j], 1);
+                mbar_init(&slot_empty[j], 1);
+            }
+        }
         fence_mbar_init();
     }
     // the allocation and the descriptor prefetches overlap the prologue's loads
@@ -214,7 +244,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
         // --------------------------------------------------- epilogue + sink
         const int q = warp & 3;
         const int epi_tid = threadIdx.x - 64;
-        const uint32_t stg = smem_u32(smem + L::kOffStaging + (warp - 2) * L::kWarpStaging);
+        // this output warp's staging slots (one, or two with send warps)
+        const uint32_t stg =
+            smem_u32(smem + L::kOffStaging + (warp - 2) * L::kSlots * L::kWarpStaging);
         uint64_t *trace = epi_tid == 0 ? trace_block(p) : nullptr;
         if (trace)
             trace[1] = globaltimer_ns();
@@ -224,8 +256,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
             acc_empty_lead[a] = mapa_shared(smem_u32(&acc_empty[a]), 0);
 
         bool ok = true;
-        bool push_ok = true;
-        const bool act = p.act_swiglu != 0;  // gated-MLP epilogue (local C only)
+        bool push_ok = true;  // SEND: every wait of this warp for a free slot succeeded
+        int k_sub = 0;        // SEND: sub-tiles this warp has handed to its send warp
+        const bool act = SEND == 0 && p.act_swiglu != 0;  // gated-MLP epilogue (local C only)
         int i = 0;
         for (int t = pair; t < total_tiles; t += n_pairs, ++i) {
             const TileCoord c =
@@ -274,6 +307,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
                     tmem_regs_ready(v0);
                     tmem_regs_ready(v1);
                 }
+                const int col_byte = (c.nb * (act ? BN / 2 : BN) + sub * 64) * 2;
+                uint32_t buf = stg;
+                int slot = 0;
+                if constexpr (SEND != 0) {
+                    // wait until the send warp has drained this slot's previous contents
+                    slot = (warp - 2) * L::kSlots + (k_sub % L::kSlots);
+                    buf = stg + (k_sub % L::kSlots) * L::kWarpStaging;
+                    const uint32_t sph = (k_sub / L::kSlots) & 1;
+                    push_ok = mbar_wait(&slot_empty[slot], sph ^ 1u, p.timeout_ns, abort_flag) &&
+                              push_ok;
+                }
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     const uint32_t *v = ch < 4 ? v0 + ch * 8 : v1 + (ch - 4) * 8;
@@ -284,11 +328,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
                             make_float2(__uint_as_float(v[2 * h]), __uint_as_float(v[2 * h + 1])));
                         w[h] = *reinterpret_cast<uint32_t *>(&b);
                     }
-                    st_shared_v4(stg + lane * 128 + ((ch ^ (lane & 7)) << 4),
+                    st_shared_v4(buf + lane * 128 + ((ch ^ (lane & 7)) << 4),
                                  make_uint4(w[0], w[1], w[2], w[3]));
                 }
+                if constexpr (SEND != 0) {
+                    // hand the slot, with its rows' destinations, to the send warp
+                    meta[slot].row_base[lane] = reinterpret_cast<unsigned long long>(row_base);
+                    if (lane == 0)
+                        meta[slot].col_byte = col_byte;
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&slot_full[slot]);
+                    ++k_sub;
+                    continue;
+                }
                 __syncwarp();
-                const int col_byte = (c.nb * (act ? BN / 2 : BN) + sub * 64) * 2;
 #pragma unroll
                 for (int it = 0; it < 8; ++it) {
                     const int row = it * 4 + (lane >> 3);
@@ -307,7 +361,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
             if (lane == 0)
                 mbar_arrive_cluster(acc_empty_lead[as]);
 
-            if (p.sink_enabled) {
+            if (SEND != 0) {
+                // the send warps hand the tile to the completion warp; a failed wait
+                // for a slot is voted on at the next tile (or reported after the loop)
+                push_ok = __all_sync(0xffffffffu, push_ok);
+            } else if (p.sink_enabled) {
                 named_bar_sync(1, 128);
                 if (epi_tid == 0) {
                     if (rec)
@@ -325,17 +383,77 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
         if (epi_tid == 0) {
             if (trace)
                 trace[0] = static_cast<uint64_t>(i);
-            close_queue(sh);
-            if (!push_ok)
-                raise_abort(p.status, abort_flag);
+            if (SEND == 0)
+                close_queue(sh);
         }
-        if (!ok && lane == 0)
+        if ((!ok || !push_ok) && lane == 0)
             raise_abort(p.status, abort_flag);
-    } else {
+    } else if (warp == 6) {
         // ------------------------------------------- completion counting + signalling
         if (lane == 0 && p.sink_enabled)
             completion_loop(p, sh);
         __syncwarp();
+    } else if constexpr (SEND != 0) {
+        // ------------------------------------------------------------ send warps
+        // Send warp sw drains the slots of output warp sw in order: each row's 128
+        // bytes of a sub-tile leave as one contiguous segment (8 lanes per row). After
+        // a tile's last sub-tile the send warps meet at a barrier, which is also their
+        // vote, and one thread hands this CTA's half of the tile to the completion warp.
+        const int sw = warp - 7;
+        const int send_tid = threadIdx.x - 224;
+        uint64_t *trace = send_tid == 0 ? trace_block(p) : nullptr;
+        bool ok = true;
+        bool push_ok = true;  // send_tid 0: the last hand-off succeeded
+        int k = 0;
+        int i = 0;
+        for (int t = pair; t < total_tiles; t += n_pairs, ++i) {
+            const TileCoord c =
+                decode_tile(t, sh->tile_start, sh->eoff, El, p.n_blocks, L::kTileRows, p.m_fastest);
+            for (int sub = 0; sub < BN / 64; ++sub, ++k) {
+                const int slot = sw * L::kSlots + (k % L::kSlots);
+                const uint32_t sph = (k / L::kSlots) & 1;
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&slot_full[slot], sph, p.timeout_ns, abort_flag));
+                if (!ok)
+                    break;
+                const uint32_t buf = smem_u32(smem + L::kOffStaging + slot * L::kWarpStaging);
+                const int col_byte = meta[slot].col_byte;
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int row = it * 4 + (lane >> 3);
+                    const int ch = lane & 7;
+                    const unsigned long long base = meta[slot].row_base[row];
+                    const uint4 val = ld_shared_v4(buf + row * 128 + ((ch ^ (row & 7)) << 4));
+                    if (base != 0ull)
+                        st_global_v4(reinterpret_cast<uint8_t *>(base) + col_byte + ch * 16, val);
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&slot_empty[slot]);
+            }
+            // every send thread's stores of this tile precede the hand-off
+            ok = named_bar_and(3, 32 * SEND, ok && push_ok);
+            if (!ok)
+                break;
+            if (send_tid == 0) {
+                uint64_t *rec = (trace && i < p.trace_records) ? trace + 2 + 4 * i : nullptr;
+                if (p.sink_enabled) {
+                    if (rec)
+                        rec[2] = globaltimer_ns();
+                    // each CTA counts its half of every pair tile of the expert
+                    const int tiles_e =
+                        2 * ((c.m_end - sh->eoff[c.e] + L::kTileRows - 1) / L::kTileRows) *
+                        p.n_blocks;
+                    push_ok = push_tile_done(p, sh, c.e, rec ? i : -1, tiles_e);
+                } else if (rec) {
+                    rec[2] = rec[3] = globaltimer_ns();
+                }
+            }
+        }
+        if (send_tid == 0)
+            close_queue(sh);
+        if ((!ok || !push_ok) && lane == 0)
+            raise_abort(p.status, abort_flag);
     }
 
     // a combine launched behind this kernel may start now: it reads nothing before
@@ -350,13 +468,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224, 1)
     }
 }
 
-cudaError_t launch_gemm_send_bf16_pair(const CUtensorMap &ta, const CUtensorMap &tb,
-                                       const SendParams &p, int max_pairs, cudaStream_t s)
+template <int SEND>
+static cudaError_t launch_pair(const CUtensorMap &ta, const CUtensorMap &tb, const SendParams &p,
+                               int max_pairs, cudaStream_t s)
 {
-    using L = PairLayout;
-    cudaError_t err = cudaFuncSetAttribute(gemm_send_bf16_pair_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           L::kSmemBytes);
+    using L = PairLayout<SEND>;
+    auto kern = gemm_send_bf16_pair_kernel<SEND>;
+    cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (err != cudaSuccess)
         return err;
     // persistent: as many pairs as can be resident at once (clusters are placed
@@ -367,14 +486,21 @@ cudaError_t launch_gemm_send_bf16_pair(const CUtensorMap &ta, const CUtensorMap 
     cfg.dynamicSmemBytes = L::kSmemBytes;
     cfg.stream = s;
     int active = 0;
-    if (cudaOccupancyMaxActiveClusters(&active, gemm_send_bf16_pair_kernel, &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess ||
         active < 1) {
         (void)cudaGetLastError();
         active = max_pairs;
     }
     const int pairs = active < max_pairs ? active : max_pairs;
-    return launch_send_kernel(gemm_send_bf16_pair_kernel, 2 * pairs, L::kThreads, L::kSmemBytes,
-                              ta, tb, p, s);
+    return launch_send_kernel(kern, 2 * pairs, L::kThreads, L::kSmemBytes, ta, tb, p, s);
+}
+
+cudaError_t launch_gemm_send_bf16_pair(const CUtensorMap &ta, const CUtensorMap &tb,
+                                       const SendParams &p, int send_warps, int max_pairs,
+                                       cudaStream_t s)
+{
+    return send_warps == 4 ? launch_pair<4>(ta, tb, p, max_pairs, s)
+                           : launch_pair<0>(ta, tb, p, max_pairs, s);
 }
 
 }  // namespace ep

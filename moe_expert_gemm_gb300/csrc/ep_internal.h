@@ -144,7 +144,8 @@ cudaError_t launch_gemm_send_bf16(const CUtensorMap &ta, const CUtensorMap &tb,
 cudaError_t launch_gemm_send_fp8(const CUtensorMap &ta, const CUtensorMap &tb,
                                  const SendParams &p, int bn, int grid, cudaStream_t s);
 cudaError_t launch_gemm_send_bf16_pair(const CUtensorMap &ta, const CUtensorMap &tb,
-                                       const SendParams &p, int max_pairs, cudaStream_t s);
+                                       const SendParams &p, int send_warps, int max_pairs,
+                                       cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_scatter(const ScatterParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_dispatch_gather(const DispatchParams &p, int num_sms, cudaStream_t s);

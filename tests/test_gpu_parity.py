@@ -254,6 +254,9 @@ SEND_WARP_CASES = [
                             "softmax_sel", 63)),
     ("qwen_shape_small", Workload("sw_qwen", 8, 16, 8, 48, 1536, 4096, "bf16", "zipf",
                                   "softmax_sel", 64)),
+    # CTA pairs with send warps: several pair tiles per pair, ragged row blocks
+    ("pair_many_tiles", Workload("sw_pair_many", 8, 2, 2, 1000, 512, 1024, "bf16", "biased",
+                                 "softmax_sel", 66)),
 ]
 
 
