@@ -197,7 +197,7 @@ def test_local_store_when_sink_disabled(send_warps):
 
 
 @pytest.mark.parametrize("N,T,pair,send_warps", [(384, 300, False, -1), (512, 600, True, -1),
-                                                 (512, 600, False, 4)])
+                                                 (512, 600, True, 4), (384, 300, False, 4)])
 def test_trace_records_every_tile_once(N, T, pair, send_warps):
     """Optional per-tile timestamps: every tile appears once per CTA that works on
     it (single CTAs: once; 256-column bf16 tiles on CTA pairs: once per CTA of the
