@@ -286,17 +286,29 @@ def test_dedicated_send_warps_two_epochs_and_empty_experts():
 
 FP8_ROW_BLOCK_CASES = [
     # several 128-row blocks per expert with ragged last blocks; zipf routing leaves
-    # experts empty; 256- and 128-column tiles
+    # experts empty; 256- and 128-column tiles; one K block; eight ranks
     ("bn256_zipf_empty", Workload("fp8_rb_zipf", 4, 4, 4, 300, 256, 768, "fp8_1d2d", "zipf",
                                   "sigmoid_sel", 57)),
     ("bn128_ragged", Workload("fp8_rb_128", 2, 2, 2, 300, 256, 384, "fp8_1d2d", "uniform",
                               "sigmoid_sel", 58)),
+    ("pair_one_k_block", Workload("fp8_p1k", 2, 3, 2, 500, 128, 256, "fp8_1d2d", "uniform",
+                                  "sigmoid_sel", 84)),
+    ("pair_eight_ranks", Workload("fp8_p8", 8, 4, 4, 300, 256, 384, "fp8_1d2d", "biased",
+                                  "sigmoid_sel", 85)),
 ]
 
 
 @pytest.mark.parametrize("name,w", FP8_ROW_BLOCK_CASES, ids=[c[0] for c in FP8_ROW_BLOCK_CASES])
 def test_fp8_row_block_parity(name, w):
     _check_full(w)
+
+
+def test_fp8_many_rows_per_expert_signal_modes():
+    """Blockwise fp8 with several row blocks per expert under per-expert signals, and
+    with the sink disabled (rows to a local C, then ep_scatter_send)."""
+    w = Workload("fp8_modes", 4, 2, 2, 400, 256, 512, "fp8_1d2d", "zipf", "sigmoid_sel", 86)
+    _check_full(w, per_expert=True)
+    _check_full(w, unfused=True)
 
 
 @pytest.mark.parametrize("T", [100, 600])  # one / several row blocks per expert
