@@ -178,7 +178,11 @@ int ep_plan(const ep_config *cfg, const int32_t *topk_ids, const ep_plan_out *ou
  *                    count word holds (epoch mod 2^32) << 32 | rows and the flag words
  *                    are not written.
  *   atomic_counter   [E_l] int32 tile-completion counters of my_rank's experts
- *   rank_completion_counter  [n_ranks] int32 election counters, one per destination
+ *   rank_completion_counter  [n_ranks] int32 election counters. In one call every
+ *                    expert's completion signals every destination (count 0 for an
+ *                    empty segment), so the per-destination counters would always
+ *                    hold the same value: element 0 elects the last expert for all
+ *                    destinations, the other elements are not used.
  *                    Both counter arrays must be zero before the first call; every
  *                    call that completes without a status bit leaves them at zero.
  *   epoch            value released into the rank flags (or the count words' high
@@ -253,11 +257,11 @@ typedef struct {
  * the receive buffer of the rank that owns each row's token. No local C tensor
  * exists ("EpiloguePeerSink" Enabled: the local store and its TMA descriptor are
  * dead).
- * EP_SIGNAL_RANK_FLAG: when the last tile of expert e is done, for every destination
- * rank dst: a plain store of the count word, then an acquire-release increment of
- * rank_completion_counter[dst]; the call that sees E_l-1 release-stores (system
- * scope) `epoch` into dst's flag word for my_rank ("ep_signal_completion",
- * ep_ord_r with has_rank_flag). EP_SIGNAL_PER_EXPERT: the count words, tagged with
+ * EP_SIGNAL_RANK_FLAG: the count words are plain progress stores (made once, at the
+ * start of the call, before any release); when the last tile of expert e is done,
+ * an acquire-release increment of the election counter; the completion that sees
+ * E_l-1 release-stores (system scope) `epoch` into every destination's flag word for
+ * my_rank ("ep_signal_completion", ep_ord_r with has_rank_flag). EP_SIGNAL_PER_EXPERT: the count words, tagged with
  * the epoch, are released for each expert; no election, no flag. Experts with no
  * rows signal count 0.
  */

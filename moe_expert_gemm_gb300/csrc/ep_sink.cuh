@@ -38,22 +38,25 @@ __device__ __forceinline__ void raise_abort(uint32_t *status, volatile int *abor
     *abort_flag = 1;
 }
 
-// Completion signalling ("ep_signal_completion", ep_ord_r with has_rank_flag) is
-// split in three steps so that the completion of the last expert, which ends the
-// call, waits on as few fences as possible:
-//  1. store_counts: the plain progress stores of expert e's count words, one per
-//     destination (values from shared memory, so no load sits between them);
-//  2. the caller's gpu-scope acquire-release fence: it acquires the expert's other
-//     tiles (whose rows the other blocks released before their tile-counter
-//     increments) and releases every row and count word of the expert into the
-//     election counters' modification order;
-//  3. elect_and_publish: the increments of the per-destination election counters
-//     (this GPU's memory, updated only by this GPU's blocks, so gpu-scope RMWs,
-//     made acquire-release by the fences around them); the block that makes a
-//     counter reach E_l has acquired every other expert's release through that RMW
-//     chain, and its one system-scope fence is the single system-scope release that
-//     carries the whole rank (cumulatively) to the peers with the rank flag. It
-//     re-arms the counter and publishes the flag.
+// Completion signalling ("ep_signal_completion", ep_ord_r with has_rank_flag) is a
+// chain of acquire-release steps kept as short as possible, because the completion
+// of the last expert ends the call:
+//  1. the count words are plain progress stores whose values the plan fixes, so block
+//     0's completion thread stores all of them (store_counts, every expert) before
+//     its first release; every release after that (its tile-counter RMWs, then the
+//     election) carries them to whoever acquires;
+//  2. each finished tile: one acquire-release RMW on its expert's tile counter
+//     (gpu scope: all producers of the rank share its GPU), which releases the
+//     tile's rows (stored by the output warps before the hand-off) and, for the
+//     tile that completes the expert, acquires every other tile of it;
+//  3. elect_and_publish, once per completed expert: one acquire-release RMW on the
+//     election counter. In one fused call every expert completion signals every
+//     destination (empty segments with count 0), so the per-destination counters
+//     of the pages would move in lockstep: counter 0 elects the last expert for all
+//     destinations at once. The elected block has acquired every other expert's
+//     release through that RMW chain; its one system-scope fence is the single
+//     system-scope release that carries the whole rank (cumulatively) to the peers,
+//     followed by the rank flag of every destination. It re-arms the counter.
 __device__ __forceinline__ void store_counts(const SendParams &p, const SinkShared *sh, int e)
 {
     const int R = p.n_ranks;
@@ -93,29 +96,18 @@ __device__ __forceinline__ void store_tagged_counts(const SendParams &p, const S
 
 static __device__ __noinline__ void elect_and_publish(const SendParams &p, const SinkShared *sh)
 {
+    const int old = atom_add_acq_rel_gpu(&p.rank_counter[0], 1);
+    if (old != p.El - 1)
+        return;
+    // last expert of this rank: re-arm the counter for the next call and publish the
+    // whole rank through the rank flag of every destination
+    *reinterpret_cast<volatile int *>(&p.rank_counter[0]) = 0;
+    fence_acq_rel_sys();
     const int R = p.n_ranks;
-    int old[EP_MAX_RANKS];
 #pragma unroll
     for (int dst = 0; dst < EP_MAX_RANKS; ++dst)
         if (dst < R)
-            old[dst] = atom_add_relaxed_gpu(&p.rank_counter[dst], 1);
-    bool elected = false;
-#pragma unroll
-    for (int dst = 0; dst < EP_MAX_RANKS; ++dst)
-        elected |= dst < R && old[dst] == p.El - 1;
-    if (!elected)
-        return;
-    fence_acq_rel_sys();
-#pragma unroll
-    for (int dst = 0; dst < EP_MAX_RANKS; ++dst) {
-        if (dst < R && old[dst] == p.El - 1) {
-            // last expert of this rank for dst: re-arm the counter for the next call and
-            // publish the whole rank through the rank flag
-            *reinterpret_cast<volatile int *>(&p.rank_counter[dst]) = 0;
-            st_relaxed_sys_u64(sh->cnt[dst] + static_cast<int64_t>(p.El) * R + p.my_rank,
-                               p.epoch);
-        }
-    }
+            st_relaxed_sys_u64(sh->cnt[dst] + static_cast<int64_t>(p.El) * R + p.my_rank, p.epoch);
 }
 
 struct TileCoord {
@@ -290,11 +282,11 @@ __device__ __forceinline__ void close_queue(SinkShared *sh)
     *reinterpret_cast<volatile int *>(&sh->q_done) = 1;
 }
 
-// Completion warp, one thread: counts finished tiles per expert (one gpu-scope
-// release fence per batch of tiles) and runs the signalling of every expert this
-// block completes (rank flag: count stores, one gpu-scope acquire-release fence for
-// the batch, election; per expert: one system-scope fence, tagged count words).
-// Block 0 also signals the experts without rows, which have no tile to complete.
+// Completion warp, one thread: counts finished tiles per expert (one acquire-release
+// RMW per tile) and runs the signalling of every expert this block completes (rank
+// flag: the election; per expert: one system-scope fence, tagged count words). Block
+// 0 first stores every count word of the rank (rank flag) and signals the experts
+// without rows, which have no tile to complete.
 static __device__ void completion_loop(const SendParams &p, SinkShared *sh)
 {
     volatile int *head_p = &sh->q_head;
@@ -304,19 +296,16 @@ static __device__ void completion_loop(const SendParams &p, SinkShared *sh)
     uint64_t *trace = trace_block(p);
     const bool per_expert = p.signal_mode == EP_SIGNAL_PER_EXPERT;
     if (blockIdx.x == 0) {
+        // every count word of the rank, before this thread's first release
+        if (!per_expert)
+            for (int e = 0; e < p.El; ++e)
+                store_counts(p, sh, e);
         bool any_empty = false;
-        for (int e = 0; e < p.El; ++e) {
-            if (sh->eoff[e + 1] == sh->eoff[e]) {
-                if (!per_expert)
-                    store_counts(p, sh, e);
-                any_empty = true;
-            }
-        }
+        for (int e = 0; e < p.El; ++e)
+            any_empty |= sh->eoff[e + 1] == sh->eoff[e];
         if (any_empty) {
             if (per_expert)
                 fence_acq_rel_sys();
-            else
-                fence_acq_rel_gpu();
             for (int e = 0; e < p.El; ++e) {
                 if (sh->eoff[e + 1] == sh->eoff[e]) {
                     if (per_expert)
@@ -339,28 +328,20 @@ static __device__ void completion_loop(const SendParams &p, SinkShared *sh)
                 ent[n++] = sh->queue[(head++) % kQueue];
             __threadfence_block();
             *head_p = head;
-            // one release fence covers the rows of every tile popped here
-            fence_acq_rel_gpu();
+            // each tile's rows released into its expert's tile counter; the tile that
+            // completes the expert acquires the expert's other tiles
             bool last[8];
             bool any = false;
             for (int j = 0; j < n; ++j) {
-                const int old = atom_add_relaxed_gpu(&p.atomic_counter[ent[j].x], 1);
+                const int old = atom_add_acq_rel_gpu(&p.atomic_counter[ent[j].x], 1);
                 last[j] = old == ent[j].z - 1;
                 any |= last[j];
             }
-            if (any) {
-                // acquire the experts' other tiles; release their rows (and counts):
-                // per expert, to the peers directly (each count word is a system-scope
-                // release); with the rank flag, to the election on this GPU
-                if (per_expert) {
-                    fence_acq_rel_sys();
-                } else {
-                    for (int j = 0; j < n; ++j)
-                        if (last[j])
-                            store_counts(p, sh, ent[j].x);
-                    fence_acq_rel_gpu();
-                }
-            }
+            // per expert: the completed experts' rows go to the peers directly (each
+            // count word is a system-scope release); with the rank flag, the election
+            // releases them on this GPU
+            if (any && per_expert)
+                fence_acq_rel_sys();
             for (int j = 0; j < n; ++j) {
                 if (last[j]) {
                     *reinterpret_cast<volatile int *>(&p.atomic_counter[ent[j].x]) = 0;

@@ -2,24 +2,27 @@
  * The completion-signalling protocol on host threads (C11 atomics), for the
  * orderings the kernels rely on. Producer threads stand for the thread blocks: tile t
  * of expert e of rank r writes its share of the expert's rows into every
- * destination's buffer, takes a release fence and increments the expert's tile
- * counter; the one that completes the expert (sees TILES - 1) takes an
- * acquire-release fence (the other tiles' rows), re-arms the tile counter and then
- *   rank-flag mode ("ep_signal_completion", ep_ord_r with has_rank_flag):
- *     stores the count words as plain (relaxed) stores, takes an acquire-release
- *     fence and increments the election counter of each destination; the producer
- *     that sees E_l - 1 takes another acquire-release fence, re-arms the counter and
- *     stores the rank flag;
+ * destination's buffer and increments the expert's tile counter with an
+ * acquire-release RMW; the one that completes the expert (sees TILES - 1) re-arms
+ * the tile counter and then
+ *   rank-flag mode ("ep_signal_completion", ep_ord_r with has_rank_flag): the count
+ *     words are plain (relaxed) stores made at the start of the call by the thread
+ *     standing for block 0 of the rank (tile 0 of expert 0), before its own release;
+ *     the completer increments the rank's election counter with an acquire-release
+ *     RMW (every expert completion signals every destination, so one counter serves
+ *     all of them); the producer that sees E_l - 1 re-arms it, takes a release fence
+ *     and stores the rank flag of every destination;
  *     a consumer per destination waits for each source rank's flag, takes an
  *     acquire fence and reads every row and count word of that rank;
- *   per-expert mode: stores each count word tagged with the epoch (after that
- *     fence); the consumer acquires each expert's word and reads that expert's rows.
+ *   per-expert mode: takes a release fence and stores each count word tagged with
+ *     the epoch; the consumer acquires each expert's word and reads that expert's rows.
  * Threads sleep for random short spans between steps, so the interleavings vary
  * with the seed. Every wait is bounded; a producer told to fail never signals.
  *
  * usage: protocol_model R E TILES ROWS EPOCHS MODE SEED [FAIL_RANK FAIL_EXPERT]
- *   MODE 0 rank flag, 1 per expert, 2 a planted mistake: the rank flag is stored by
- *   the first expert to finish instead of the last (the checks must catch it).
+ *   MODE 0 rank flag, 1 per expert, and two planted mistakes the checks must catch:
+ *   2 the rank flag is stored by the first expert to finish instead of the last;
+ *   3 block 0 stores the count words after its release instead of before it.
  *   Prints one line:
  *   "epochs N errors X timeouts Y elections Z" (Z = elections over all epochs).
  */
@@ -40,7 +43,7 @@ static const double TIMEOUT_S = 0.05;
 static _Atomic uint64_t payload[MAX_R][MAX_R][MAX_E][MAX_ROWS]; /* [dst][src][e][row] */
 static _Atomic uint64_t counts[MAX_R][MAX_E * MAX_R];            /* [dst][e*R + src] */
 static _Atomic uint64_t flags[MAX_R][MAX_R];                     /* [dst][src] */
-static _Atomic int rank_counter[MAX_R][MAX_R];                   /* [src][dst] */
+static _Atomic int rank_counter[MAX_R];                          /* [src] */
 static _Atomic int tile_counter[MAX_R][MAX_E];                   /* [src][e] */
 static atomic_int errors, timeouts, elections;
 static pthread_barrier_t epoch_bar;
@@ -82,8 +85,16 @@ static void *producer_main(void *arg)
 {
     const struct producer *p = arg;
     uint64_t rng = SEED ^ mix((uint64_t)((p->src * MAX_E + p->e) * MAX_TILES + p->tile + 1));
+    const int block0 = p->e == 0 && p->tile == 0;  /* stands for block 0 of the rank */
     for (int ep = 1; ep <= EPOCHS; ++ep) {
         pthread_barrier_wait(&epoch_bar);
+        if (block0 && (MODE == 0 || MODE == 2)) {  /* every count word, before any release */
+            for (int dst = 0; dst < R; ++dst)
+                for (int e = 0; e < E; ++e)
+                    atomic_store_explicit(&counts[dst][e * R + p->src], (uint64_t)ROWS + (uint64_t)ep,
+                                          memory_order_relaxed);
+            jitter(&rng);
+        }
         for (int dst = 0; dst < R; ++dst) {
             for (int i = p->tile; i < ROWS; i += TILES)
                 atomic_store_explicit(&payload[dst][p->src][p->e][i], row_value(ep, dst, p->src, p->e, i),
@@ -92,45 +103,38 @@ static void *producer_main(void *arg)
         }
         const int fail = p->src == FAIL_R && p->e == FAIL_E;
         int completes = 0;
-        if (!fail) {
-            atomic_thread_fence(memory_order_release);
-            completes = atomic_fetch_add_explicit(&tile_counter[p->src][p->e], 1, memory_order_relaxed) ==
+        if (!fail)
+            completes = atomic_fetch_add_explicit(&tile_counter[p->src][p->e], 1, memory_order_acq_rel) ==
                         TILES - 1;
-        }
         if (completes) {
-            atomic_thread_fence(memory_order_acq_rel);
             atomic_store_explicit(&tile_counter[p->src][p->e], 0, memory_order_relaxed);
             jitter(&rng);
-            if (MODE == 0 || MODE == 2) {
-                const int last = MODE == 0 ? E - 1 : 0;
-                for (int dst = 0; dst < R; ++dst)
-                    atomic_store_explicit(&counts[dst][p->e * R + p->src], (uint64_t)ROWS + (uint64_t)ep,
-                                          memory_order_relaxed);
-                jitter(&rng);
-                atomic_thread_fence(memory_order_acq_rel);
-                int old[MAX_R];
-                for (int dst = 0; dst < R; ++dst)
-                    old[dst] = atomic_fetch_add_explicit(&rank_counter[p->src][dst], 1, memory_order_relaxed);
-                int elected = 0;
-                for (int dst = 0; dst < R; ++dst)
-                    elected |= old[dst] == last;
-                if (elected) {
-                    atomic_thread_fence(memory_order_acq_rel);
+            if (MODE != 1) {
+                const int last = MODE == 2 ? 0 : E - 1;
+                const int old = atomic_fetch_add_explicit(&rank_counter[p->src], 1, memory_order_acq_rel);
+                if (old == E - 1)  /* the last increment re-arms the counter */
+                    atomic_store_explicit(&rank_counter[p->src], 0, memory_order_relaxed);
+                if (old == last) {
+                    atomic_thread_fence(memory_order_release);
                     for (int dst = 0; dst < R; ++dst) {
-                        if (old[dst] != last)
-                            continue;
                         atomic_fetch_add(&elections, 1);
                         atomic_store_explicit(&flags[dst][p->src], (uint64_t)ep, memory_order_relaxed);
                     }
                 }
-                for (int dst = 0; dst < R; ++dst)  /* the last increment re-arms the counter */
-                    if (old[dst] == E - 1)
-                        atomic_store_explicit(&rank_counter[p->src][dst], 0, memory_order_relaxed);
             } else {
+                atomic_thread_fence(memory_order_release);
                 for (int dst = 0; dst < R; ++dst)
                     atomic_store_explicit(&counts[dst][p->e * R + p->src],
                                           ((uint64_t)ep << 32) | (uint64_t)ROWS, memory_order_relaxed);
             }
+        }
+        if (block0 && MODE == 3) {  /* planted: the count words after this block's release */
+            jitter(&rng);
+            jitter(&rng);
+            for (int dst = 0; dst < R; ++dst)
+                for (int e = 0; e < E; ++e)
+                    atomic_store_explicit(&counts[dst][e * R + p->src], (uint64_t)ROWS + (uint64_t)ep,
+                                          memory_order_relaxed);
         }
         pthread_barrier_wait(&epoch_bar); /* every consumer has finished the epoch */
     }

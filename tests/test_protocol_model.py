@@ -1,16 +1,18 @@
 """The completion-signalling protocol run by host threads with C11 atomics
 (`protocol_model.c`): producer threads play the thread blocks of every rank's
 experts (several tiles per expert), consumer threads the destination ranks. The
-orderings are those of the kernels: tile rows released into a per-expert tile
-counter; the expert's completer stores its count words and increments the
-election counters under acquire-release fences; the elected producer releases the
-rank flag ("ep_signal_completion", ep_ord_r with has_rank_flag), or every count
-word is tagged with the epoch (per-expert mode). Across many epochs and seeded
-interleavings every consumer that acquires a signal sees all the rows and counts
-it covers, exactly one producer per (source, destination) is elected, a producer
-that never signals makes the waits run out instead of hanging, and a planted
-mistake (a flag released by the first expert instead of the last) is caught. On
-an Arm host (weakly ordered) the fences are exercised as well as the logic."""
+orderings are those of the kernels: the count words stored at the start by the
+rank's block 0, before its release; tile rows released into a per-expert tile
+counter by acquire-release RMWs; the expert's completer increments the rank's
+election counter with an acquire-release RMW; the elected producer releases the
+rank flag of every destination ("ep_signal_completion", ep_ord_r with
+has_rank_flag), or every count word is tagged with the epoch (per-expert mode).
+Across many epochs and seeded interleavings every consumer that acquires a signal
+sees all the rows and counts it covers, exactly one producer per (source,
+destination) is elected, a producer that never signals makes the waits run out
+instead of hanging, and two planted mistakes (a flag released by the first expert
+instead of the last; the count words stored after block 0's release) are caught.
+On an Arm host (weakly ordered) the fences are exercised as well as the logic."""
 
 import os
 import shutil
@@ -68,3 +70,8 @@ def test_a_producer_that_never_signals_makes_the_waits_run_out(model, mode):
 def test_the_checks_catch_a_flag_released_too_early(model):
     got = run(model, 4, 3, 2, 48, 150, 2, 9)
     assert got["errors"] > 0
+
+
+def test_the_checks_catch_count_words_stored_after_the_release(model):
+    got = sum(run(model, 4, 3, 2, 48, 150, 3, seed)["errors"] for seed in (9, 10, 11))
+    assert got > 0
