@@ -297,6 +297,16 @@ int prepare_send(const ep_config *cfg, const ep_send_args *a, PreparedSend *out)
     p.trace = a->trace;
     p.trace_records = a->trace ? static_cast<int>(a->trace_records) : 0;
     p.overlap_previous = a->overlap_previous ? 1 : 0;
+    // sink disabled ("EpiloguePeerSink" disabled: the local C store is the epilogue's
+    // own): the bf16 output warps store whole 32-row groups of C with TMA
+    if (!sink && !fp8 && cfg->send_warps != 4) {
+        const int64_t c_cols = p.c_row_bytes / 2;
+        if (!encode_2d(&p.tmap_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->C,
+                           static_cast<uint64_t>(c_cols), static_cast<uint64_t>(a->max_rows),
+                           static_cast<uint64_t>(p.c_row_bytes), 64, 32))
+            return EP_ERR_CUDA;
+        p.c_tma = 1;
+    }
 
     // the plan lives on the device, so size the grid by the worst-case tile count
     const int64_t max_tiles = ((a->max_rows + ep::BM - 1) / ep::BM + El) * p.n_blocks;

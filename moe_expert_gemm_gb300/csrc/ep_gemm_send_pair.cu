@@ -318,6 +318,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224 + 32 * SEND, 1)
                     push_ok = mbar_wait(&slot_empty[slot], sph ^ 1u, p.timeout_ns, abort_flag) &&
                               push_ok;
                 }
+                // sink disabled, whole 32-row groups of the expert leave as one TMA store
+                // from the staging buffer (the map's 128-byte swizzle is the buffer's);
+                // the previous store of this warp must have read the buffer
+                const int group_row = c.m_abs + static_cast<int>(rank) * BM + q * 32;
+                const bool tma_group = SEND == 0 && p.c_tma && group_row + 32 <= c.m_end;
+                if (SEND == 0 && p.c_tma) {
+                    if (lane == 0)
+                        bulk_wait_read_all();
+                    __syncwarp();
+                }
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     const uint32_t *v = ch < 4 ? v0 + ch * 8 : v1 + (ch - 4) * 8;
@@ -340,6 +350,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224 + 32 * SEND, 1)
                     if (lane == 0)
                         mbar_arrive(&slot_full[slot]);
                     ++k_sub;
+                    continue;
+                }
+                if (tma_group) {
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&p.tmap_c, buf, col_byte / 2, group_row);
+                        bulk_commit();
+                    }
                     continue;
                 }
                 __syncwarp();
@@ -380,6 +399,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(224 + 32 * SEND, 1)
                 rec[2] = rec[3] = globaltimer_ns();
             }
         }
+        // the local C's TMA stores have completed before the block ends
+        if (SEND == 0 && p.c_tma && lane == 0)
+            bulk_wait_all();
         if (epi_tid == 0) {
             if (trace)
                 trace[0] = static_cast<uint64_t>(i);

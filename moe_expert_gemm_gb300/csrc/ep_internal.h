@@ -13,8 +13,12 @@ namespace ep {
 constexpr int BM = 128;          // rows per tile (tcgen05 M, one TMEM lane per row)
 constexpr int kRowBytesK = 128;  // bytes of K per stage and row: one 128-byte swizzle atom
 
-// Everything the fused GEMM + send kernel reads besides the two tensor maps.
+// Everything the fused GEMM + send kernel reads besides the two operand tensor maps.
 struct SendParams {
+    // sink disabled (bf16 kernels, output warps storing): the local C as a tensor map,
+    // box 64 columns x 32 rows with the 128-byte swizzle of the staging buffers
+    CUtensorMap tmap_c;
+    int c_tma;         // tmap_c is valid
     int n_ranks, my_rank, El, top_k, K, N, max_tokens;
     int n_blocks;      // column blocks per expert (N / BN)
     int m_fastest;     // tile order within an expert: row blocks fastest (else column blocks)

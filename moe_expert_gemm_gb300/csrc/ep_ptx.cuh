@@ -141,6 +141,24 @@ __device__ __forceinline__ void bulk_wait_all()
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// 2-D tiled store of a shared-memory box to global memory through a tensor map (the
+// box's layout in shared memory is the map's swizzle), tracked in bulk groups. The
+// coordinates must be non-negative, x a multiple of 16 bytes.
+__device__ __forceinline__ void tma_store_2d(const void *map, uint32_t smem_src, int32_t x,
+                                             int32_t y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_src), "r"(x), "r"(y)
+                 : "memory");
+}
+
+// Every bulk group this thread committed has finished reading its shared memory.
+__device__ __forceinline__ void bulk_wait_read_all()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // This thread's generic-proxy shared-memory writes before async-proxy reads of them.
 __device__ __forceinline__ void fence_proxy_async_shared()
 {
