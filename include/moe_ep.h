@@ -59,9 +59,9 @@ typedef struct CUstream_st *ep_stream_t;
 
 /* completion signalling ("ep_signal_completion") */
 #define EP_SIGNAL_RANK_FLAG 0  /* ep_ord_r with has_rank_flag: plain count words, an
-                                  acquire-release election per destination, the elected
-                                  producer release-stores the rank flag; the consumer
-                                  acquires one flag per source rank */
+                                  acquire-release election, the elected producer
+                                  release-stores the rank flag of every destination; the
+                                  consumer acquires one flag per source rank */
 #define EP_SIGNAL_PER_EXPERT 1 /* the default mode: every expert's count word is its own
                                   arrival signal, released once the expert's rows are
                                   written; no election, no rank flag; the consumer
