@@ -133,13 +133,12 @@ class NvmlClocks:
                 return
             self.lib = lib
             self.handle = self._find_handle(device_index)
+            reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            self.reasons_fn = reasons or lib.nvmlDeviceGetCurrentClocksThrottleReasons
         except (OSError, AttributeError):
             self.lib = None
         if self.handle is None:
             self.lib = None
-        else:
-            reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
-            self.reasons_fn = reasons or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
 
     def _find_handle(self, device_index: int):
         import torch
