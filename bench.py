@@ -376,8 +376,8 @@ def measure_workload(name: str, steps: int, warmup: int, peaks: dict, peak_src: 
                      device_index: int, probe_s: float = 0.5) -> dict:
     """Fused send and combine of rank 0 and of the most-loaded rank of one workload,
     every rank staged as in the headline step (serialised kernels, CUDA events on the
-    launching stream, L2 flushed between steps where the inputs fit in it), then a
-    back-to-back probe of the same step under NVML clock sampling."""
+    launching stream, L2 flushed between steps where the inputs fit in it, clocks
+    sampled), then, after both, a back-to-back probe of each under clock sampling."""
     import torch
     from moe_expert_gemm_gb300.system import EpSystem
     from synth import WORKLOADS, make_rank_values, make_routing, rows_per_rank
@@ -403,14 +403,13 @@ def measure_workload(name: str, steps: int, warmup: int, peaks: dict, peak_src: 
         raise SystemExit(f"{name}: device status after staging: {s.status_words()}")
     stream = torch.cuda.current_stream()
     epoch = [2]
-    out = {}
-    for q in targets:
+
+    def stepper(q):
+        """The step of rank q (flush where the inputs fit in L2, the peers' flags, the
+        send, the combine), with events around the send and the combine."""
         peer_idx = torch.tensor([w.n_local_experts * w.n_ranks + r for r in range(w.n_ranks)
                                  if r != q], dtype=torch.int64, device="cuda")
-        plan_q = s.plan_host(q)
-        m_rows = plan_q["m_total"]
-        flops, send_bytes, comb_bytes = algorithmic_work(w, plan_q["send_counts"], m_rows)
-        need_flush, l2_text = l2_policy(w, m_rows)
+        need_flush = l2_policy(w, int(rows[q]))[0]
         flush = torch.empty(512 * 2**20, dtype=torch.uint8, device="cuda") if need_flush else None
 
         def step(ev=None):
@@ -428,17 +427,43 @@ def measure_workload(name: str, steps: int, warmup: int, peaks: dict, peak_src: 
             s.combine(q, e, stream)
             if ev is not None:
                 ev[2].record(stream)
+        return step
 
+    out = {}
+    # every target's timed steps first (each after a short idle gap, so that no earlier
+    # sustained run holds the clocks down), then the sustained probes
+    for q in targets:
+        plan_q = s.plan_host(q)
+        m_rows = plan_q["m_total"]
+        flops, send_bytes, comb_bytes = algorithmic_work(w, plan_q["send_counts"], m_rows)
+        step = stepper(q)
         for _ in range(warmup):
             step()
         torch.cuda.synchronize()
+        time.sleep(0.2)
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        clk = clock_sampler(device_index)
+        clk.start()
+        t0 = time.perf_counter()
         for i in range(steps):
             step(evs[i])
         torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        timed_clocks = clk.stop(busy=(t0, t1))
         send_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
         comb_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+        roof = roofline(w, flops, send_bytes, send_ms / 1e3, peaks, peak_src,
+                        measured_traffic(w.name, "grouped_gemm_combine_send") if q == 0 else None)
+        out["rank0" if q == 0 else "max_rank"] = {
+            "rank": q, "rows": int(m_rows), "steps": steps, "warmup": warmup,
+            "fused_ms": send_ms, "combine_ms": comb_ms, "step_ms": send_ms + comb_ms,
+            "tokens_per_s": w.tokens / ((send_ms + comb_ms) / 1e3),
+            "tflops": flops / (send_ms / 1e3) / 1e12,
+            "combine_gbs": comb_bytes / (comb_ms / 1e3) / 1e9,
+            "roofline": roof, "l2": l2_policy(w, m_rows)[1], "clocks": timed_clocks}
+    for q in targets:
         # the same step back to back for ~probe_s, under clock sampling
+        step = stepper(q)
         clk = clock_sampler(device_index)
         clk.start()
         probe = []
@@ -453,22 +478,13 @@ def measure_workload(name: str, steps: int, warmup: int, peaks: dict, peak_src: 
         t1 = time.perf_counter()
         clocks = clk.stop(busy=(t0, t1))
         probe_send = statistics.mean(e[0].elapsed_time(e[1]) for e in probe)
-        if s.status_words().any():
-            raise SystemExit(f"{name}: device status after timing: {s.status_words()}")
-        roof = roofline(w, flops, send_bytes, send_ms / 1e3, peaks, peak_src,
-                        measured_traffic(w.name, "grouped_gemm_combine_send") if q == 0 else None)
-        entry = {"rank": q, "rows": int(m_rows), "steps": steps, "warmup": warmup,
-                 "fused_ms": send_ms, "combine_ms": comb_ms, "step_ms": send_ms + comb_ms,
-                 "tokens_per_s": w.tokens / ((send_ms + comb_ms) / 1e3),
-                 "tflops": flops / (send_ms / 1e3) / 1e12,
-                 "combine_gbs": comb_bytes / (comb_ms / 1e3) / 1e9,
-                 "roofline": roof, "l2": l2_text,
-                 "probe": {"seconds": t1 - t0, "steps": len(probe), "fused_ms": probe_send,
-                           "clocks": clocks}}
+        entry = out["rank0" if q == 0 else "max_rank"]
+        entry["probe"] = {"seconds": t1 - t0, "steps": len(probe), "fused_ms": probe_send,
+                          "clocks": clocks}
         if clocks and clocks.get("sm_mhz"):
             entry["probe"]["fused_kcycles_at_median_clock"] = probe_send * clocks["sm_mhz"]
-        out["rank0" if q == 0 else "max_rank"] = entry
-        del flush
+    if s.status_words().any():
+        raise SystemExit(f"{name}: device status after timing: {s.status_words()}")
     del s
     torch.cuda.empty_cache()
     return out
