@@ -113,7 +113,7 @@ def load_peaks():
 
 
 class NvmlClocks:
-    """Read-only NVML queries (ctypes on the driver's libnvidia-ml) of one GPU's SM
+    """Read-only NVML queries (ctypes on NVIDIA's libnvidia-ml) of one GPU's SM
     clock, clock-event reasons and power: sampled every ~2 ms on a thread while a
     timed region runs. Nothing is ever set."""
 

@@ -13,7 +13,7 @@ with the oracle's own twice-rounded value would double that bound, since two
 correctly rounded chains may land two ulps apart. Indices, counts and flags are
 compared bit for bit.
 
-The survey's own metric for combined outputs (its reading R14),
+The rms-floored metric of the received rows, applied to combined outputs,
 max_i |g_i - r_i| / max(|r_i|, rms(r)) against the exact value, is computed on
 every combined output as well and asserted at the same tolerance wherever a
 correctly rounded result can meet it: the oracle's own twice-rounded output is
@@ -64,7 +64,7 @@ def combine_rel_err(got_bits, ref_exact, rows_exact, gates) -> float:
     return float(np.max(np.abs(g - r) / den))
 
 
-def r14_rel_err(got_bits, ref) -> float:
+def rms_floored_err(got_bits, ref) -> float:
     """max_i |g_i - r_i| / max(|r_i|, rms(r)) of bf16 outputs against float64 (or
     bf16-bit) reference values r."""
     g = bf16_to_f32(got_bits).astype(np.float64)
@@ -85,18 +85,19 @@ PARITY_LOG: list = []
 def assert_combine_close(got_bits, oracle_bits, out_exact, rows_exact, gates, tol,
                          where="") -> dict:
     """Combined outputs against the oracle: the scaled bound (always), and the
-    survey's R14 metric against the exact value wherever the oracle's own
-    correctly rounded output meets it. Returns (and records) the three values."""
+    rms-floored metric against the exact value wherever the oracle's own correctly
+    rounded output meets it. Returns (and records) the three values."""
     scaled = combine_rel_err(got_bits, out_exact, rows_exact, gates)
-    r14 = r14_rel_err(got_bits, out_exact)
-    witness = r14_rel_err(oracle_bits, out_exact)
-    rec = dict(where=str(where), tol=tol, scaled=scaled, r14_exact=r14,
-               r14_oracle_rounded=witness, r14_vs_oracle=r14_rel_err(got_bits, oracle_bits),
-               r14_asserted=witness <= tol)
+    floored = rms_floored_err(got_bits, out_exact)
+    witness = rms_floored_err(oracle_bits, out_exact)
+    rec = dict(where=str(where), tol=tol, scaled=scaled, rms_floored_exact=floored,
+               rms_floored_oracle_rounded=witness,
+               rms_floored_vs_oracle=rms_floored_err(got_bits, oracle_bits),
+               rms_floored_asserted=witness <= tol)
     PARITY_LOG.append(rec)
     assert scaled <= tol, rec
     if witness <= tol:
-        assert r14 <= tol, rec
+        assert floored <= tol, rec
     return rec
 
 

@@ -1,5 +1,5 @@
 """Expert parallelism with one rank per process (GPU): every logical rank is its own
-process on the one GPU a test box offers, with its own receive buffers; the ranks
+process on one GPU, with its own receive buffers; the ranks
 exchange CUDA IPC handles of those buffers over gloo, map their peers' buffers, and
 each runs its own fused send into the mapped peer memory and its own combine
 ("ep_signal_completion": direct memory access to a device on the same node;
@@ -36,6 +36,9 @@ CASES = [
     # eight processes, 256-row CTA-pair tiles, Zipf routing
     ("pairs_8_ranks", Workload("mp_pairs", 8, 16, 8, 512, 256, 512, "bf16", "zipf",
                                "softmax_sel", 92), 0),
+    # blockwise fp8 operands (the fp8 kernel's bulk-copy rows into mapped peer memory)
+    ("fp8_rank_flag", Workload("mp_fp8", 4, 2, 2, 100, 256, 256, "fp8_1d2d", "uniform",
+                               "sigmoid_sel", 93), 0),
 ]
 
 

@@ -74,7 +74,7 @@ def test_single_process_helpers():
 
 def test_reference_arm_line_on_rank_0():
     """The reference arm's JSON line (the oracle on the host, tiny workload): the keys
-    the driver reads, its cpu_baseline describing the run, and an e2e equal to it."""
+    a harness reads, its cpu_baseline describing the run, and an e2e equal to it."""
     import json
     sys.path.insert(0, ROOT)
     import bench
