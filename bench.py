@@ -461,6 +461,9 @@ def measure_workload(name: str, steps: int, warmup: int, peaks: dict, peak_src: 
             "tflops": flops / (send_ms / 1e3) / 1e12,
             "combine_gbs": comb_bytes / (comb_ms / 1e3) / 1e9,
             "roofline": roof, "l2": l2_policy(w, m_rows)[1], "clocks": timed_clocks}
+        if timed_clocks and timed_clocks.get("sm_mhz"):
+            # the kernel's time in SM clock cycles (thousands) at the median clock sampled
+            timed_clocks["fused_kcycles_at_median_clock"] = send_ms * timed_clocks["sm_mhz"]
     for q in targets:
         # the same step back to back for ~probe_s, under clock sampling
         step = stepper(q)
@@ -904,6 +907,9 @@ def main():
                          else 3 if unfused else 2) * args.steps * (2 if overlap else 1),
         "clocks": clk,
     }
+    if clk and clk.get("sm_mhz"):
+        # the dominant kernel's time in SM clock cycles (thousands) at the median clock
+        clk["fused_kcycles_at_median_clock"] = dom_s * 1e3 * clk["sm_mhz"]
     if e2e is not None:
         line["e2e"] = e2e
     if args.solo:
