@@ -230,3 +230,55 @@ def test_binding_structs_match_the_header(tmp_path):
             d = getattr(cls, field)
             want.append(f"{name} {field} {d.offset} {d.size}")
     assert [g for g in got if g] == want
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "moe_ep.h"
+
+int main(void)
+{
+    /* the Mixtral-like down-projection of rank 0: 8 ranks x 1 expert, top-2 */
+    ep_config cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.n_ranks = 8; cfg.my_rank = 0; cfg.n_local_experts = 1; cfg.top_k = 2;
+    cfg.num_tokens = 4096; cfg.max_tokens_per_rank = 4096; cfg.K = 14336; cfg.N = 4096;
+    cfg.msg_bytes = 2 * 4096; cfg.dtype = EP_BF16; cfg.send_warps = -1;
+    cfg.signal_mode = EP_SIGNAL_RANK_FLAG;
+    int64_t rows = -1;
+    int rc = ep_plan_sizes(&cfg, &rows);
+    printf("plan_sizes %d %lld\n", rc, (long long)rows);
+    cfg.n_ranks = EP_MAX_RANKS + 1;
+    printf("too_many_ranks %d\n", ep_plan_sizes(&cfg, &rows));
+    ep_ipc_handle h;
+    printf("ipc_null %d\n", ep_ipc_export(NULL, &h));
+    printf("send_null %d\n", grouped_gemm_combine_send(NULL, NULL, NULL));
+    printf("strerror %s\n", ep_strerror(EP_ERR_UNSUPPORTED));
+    return 0;
+}
+"""
+
+
+def test_a_c_program_links_and_calls_the_library(tmp_path, lib):
+    """The boundary from plain C: a program built against include/moe_ep.h and linked
+    to libmoe_ep.so calls the host-side entry points (no GPU needed)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(ep.LIB_PATH)
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                    "-L", libdir, "-lmoe_ep", f"-Wl,-rpath,{libdir}"], check=True,
+                   capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = dict(line.split(" ", 1) for line in out if line)
+    assert got["plan_sizes"] == f"{ep.EP_OK} {4096 * 8 * 1}"
+    assert got["too_many_ranks"] == str(ep.EP_ERR_UNSUPPORTED)
+    assert got["ipc_null"] == str(ep.EP_ERR_INVALID_ARG)
+    assert got["send_null"] == str(ep.EP_ERR_INVALID_ARG)
+    assert got["strerror"] == ep.ep_strerror(ep.EP_ERR_UNSUPPORTED)
