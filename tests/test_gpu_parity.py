@@ -225,6 +225,48 @@ def test_trace_records_every_tile_once(N, T, pair, send_warps):
     assert done == [e for e in range(w.n_local_experts) if rows[e] > 0]
 
 
+def test_maximum_local_experts_parity():
+    """EP_MAX_LOCAL_EXPERTS (256) local experts in one fused call: a tile table over
+    256 experts (most with one to three rows, many empty) and E_l * R count words."""
+    w = Workload("max_el", 2, ep.EP_MAX_LOCAL_EXPERTS, 8, 64, 128, 128, "bf16", "uniform",
+                 "softmax_sel", 94)
+    _check_full(w)
+
+
+@pytest.mark.parametrize("signal_mode", [0, 1])
+def test_empty_batch_signals_every_expert_with_count_zero(signal_mode):
+    """A batch with no tokens (receive buffers sized for 16): every expert of every
+    rank still signals ("ep_signal_completion": an empty (expert, destination) segment
+    reports count 0, and the rank flag needs every expert), the combine has nothing to
+    reduce, and no receive slot is written."""
+    from moe_expert_gemm_gb300.system import EpSystem
+    R, El, k, K, N = 4, 2, 2, 128, 128
+    s = EpSystem(R, El, k, 0, K, N, "bf16", max_tokens=16, signal_mode=signal_mode)
+    s.set_routing(np.zeros((R, 0, k), np.int32))
+    for r in range(R):
+        s.plan(r)
+        s.set_operands(r, np.zeros((0, K), np.uint16), np.zeros((El, N, K), np.uint16))
+        s.set_gates(r, np.zeros((0, k), np.float32))
+    for r in range(R):
+        s.send(r, epoch=7)
+    for d in range(R):
+        s.combine(d, epoch=7)
+    torch.cuda.synchronize()
+    assert (s.status_words() == 0).all(), s.status_words()
+    for d in range(R):
+        words = s.counts[d].cpu().numpy().view(np.uint64)
+        if signal_mode == 0:
+            np.testing.assert_array_equal(words[:El * R], np.zeros(El * R, np.uint64))
+            np.testing.assert_array_equal(words[El * R:], np.full(R, 7, np.uint64))
+        else:
+            np.testing.assert_array_equal(words[:El * R], np.full(El * R, 7 << 32, np.uint64))
+        assert (s.recv[d].cpu().numpy() == 0xFF).all()  # the sentinel everywhere
+    for r in range(R):
+        assert s.plan_host(r)["m_total"] == 0
+        assert int(s.atomic_counter[r].abs().sum()) == 0
+        assert int(s.rank_counter[r].abs().sum()) == 0
+
+
 def test_pair_kernel_small_parity():
     """256-column bf16 tiles run on CTA pairs (M = 256 across two SMs) once an
     expert's expected rows fill a pair tile: ragged experts that end inside
