@@ -62,7 +62,7 @@ typedef struct CUstream_st *ep_stream_t;
                                   acquire-release election, the elected producer
                                   release-stores the rank flag of every destination; the
                                   consumer acquires one flag per source rank */
-#define EP_SIGNAL_PER_EXPERT 1 /* the default mode: every expert's count word is its own
+#define EP_SIGNAL_PER_EXPERT 1 /* without ep_ord_r: every expert's count word is its own
                                   arrival signal, released once the expert's rows are
                                   written; no election, no rank flag; the consumer
                                   acquires, per token, the words of that token's experts */
