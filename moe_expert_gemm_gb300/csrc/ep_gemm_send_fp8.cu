@@ -24,11 +24,12 @@
 //             half (w - 3) / 4; each thread keeps its row's BN/2 fp32 accumulators
 //             (as pairs, updated with paired FMAs), adds sa[m, kb] * sw[e, n/128, kb] *
 //             partial per K block, then rounds to bf16 into a shared-memory tile
-//             buffer and sends its BN/2 columns with one bulk copy (the row's bytes
-//             are contiguous at the destination). The copies run on the TMA engine
-//             while the warps promote the next tile; a tile goes to the completion
-//             warp once its copies have completed (at the next tile's epilogue, or
-//             after the last tile), so the rows it signals are written.
+//             buffer; once both halves of the tile's rows are staged, the thread of
+//             each row's first half sends the whole row (BN columns, contiguous at the
+//             destination) with one bulk copy. The copies run on the TMA engine while
+//             the warps promote the next tile; a tile goes to the completion warp once
+//             its copies have completed (at the next tile's epilogue, or after the last
+//             tile), so the rows it signals are written.
 #include <cuda_bf16.h>
 
 #include "ep_internal.h"
@@ -331,7 +332,7 @@ __global__ void __launch_bounds__(352, 1)
             named_bar_sync(1, 256);
             if (ptid == 0 && pend_e >= 0 && p.sink_enabled)
                 push_ok = push_written_tile(p, sh, trace, pend_e, i - 1) && push_ok;
-            // this thread's row in bf16 into the buffer, then one bulk copy of it
+            // this thread's half row in bf16 into the buffer
 #pragma unroll
             for (int ch = 0; ch < HC / 8; ++ch) {
                 uint32_t w[4];
@@ -346,8 +347,11 @@ __global__ void __launch_bounds__(352, 1)
                 st_shared_v4(trow + ch * 16, make_uint4(w[0], w[1], w[2], w[3]));
             }
             fence_proxy_async_shared();
-            if (row_base != nullptr)
-                bulk_store(row_base + (c.nb * BN + half * HC) * 2, trow, HC * 2);
+            // both halves of every row are staged: one copy per row (its BN columns are
+            // contiguous at the destination), issued by the thread of its first half
+            named_bar_sync(1, 256);
+            if (half == 0 && row_base != nullptr)
+                bulk_store(row_base + c.nb * BN * 2, trow, BN * 2);
             bulk_commit();
             pend_e = c.e;
             if (!p.sink_enabled && rec)
